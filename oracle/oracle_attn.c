@@ -1,0 +1,318 @@
+/*
+ * oracle_attn.c -- plain, slow, fp64 CPU oracle for exact causal grouped-query
+ * softmax attention over paged K/V.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this file's library.  It shares no code,
+ * header, table or helper with the CUDA path and must never be called by it.
+ *
+ * What it computes (one output row per (b, q head h, query row i)):
+ *
+ *   kv head       g  = h / (Hq / Hkv)                       contiguous GQA groups
+ *   visible keys  n  = L_b - q_len + i + 1                   queries are the suffix of K/V
+ *   key t < n     k_t = k_pages[page_table[b][t / P]][g][t % P][:]   (same for v)
+ *   s_t = scale * sum_d q[d] * k_t[d]
+ *   o   = sum_t exp(s_t - M) v_t / sum_t exp(s_t - M),   M = max_t s_t
+ *   lse = M + log(sum_t exp(s_t - M))
+ *
+ * Sources (page title, section):
+ *  - CFR-Atlas README, "Core contract": folded attention over exact pages must
+ *    equal full-KV attention; oracle_attn below is that full-KV definition and
+ *    oracle_folded is the page-by-page online-softmax fold that the same
+ *    README describes in its opening paragraph and in the "Attention" row of
+ *    its responsibility table.
+ *  - CFR-Atlas README, "Minimal integration": pages hold row-major K[token][dim]
+ *    and V[token][dim] per (layer, K/V head, token range).
+ *  - CPUAttn README, "Parallel example": with kv_cache=True the queries are the
+ *    suffix of K/V, so query row i sits at position SKV - SQ + i; decode is the
+ *    same pattern with one query row ("Operator model").
+ *  - CPUAttn README, "Operator model": split-K needs a structured merge;
+ *    oracle_state + oracle_merge state that merge.
+ *  - ferrox-core crate index, "attention" module: the vanilla causal GQA path
+ *    is the correctness baseline.
+ *
+ * All inputs are fp32 arrays holding the exact stored values (bf16 inputs are
+ * widened exactly by the caller); all arithmetic is fp64.
+ *
+ * Return codes: 0 ok, 1 bad argument (shape, GQA ratio), 2 a row has no
+ * visible key or its context exceeds the page table, 3 a page id is out of
+ * range, 4 out of memory.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    const float *q, *k, *v;
+    const int32_t *table, *lens;
+    int B, Hq, Hkv, D, P, max_pages, num_pages, q_len;
+    double scale;
+} problem;
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static int check_problem(const problem *p) {
+    if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->P <= 0 ||
+        p->max_pages <= 0 || p->num_pages <= 0 || p->q_len <= 0)
+        return 1;
+    if (p->Hq % p->Hkv != 0) return 1;
+    return 0;
+}
+
+/* Split a flat row index r = (b * Hq + h) * q_len + i into its parts. */
+static void row_parts(const problem *p, int64_t r, int *b, int *h, int *i) {
+    *i = (int)(r % p->q_len);
+    *h = (int)((r / p->q_len) % p->Hq);
+    *b = (int)(r / ((int64_t)p->q_len * p->Hq));
+}
+
+/* Number of keys row (b, i) may see, or -1 if the row is invalid. */
+static int64_t visible_keys(const problem *p, int b, int i) {
+    int64_t L = p->lens[b];
+    if (L > (int64_t)p->max_pages * p->P) return -1;
+    int64_t n = L - p->q_len + i + 1;
+    return n >= 1 ? n : -1;
+}
+
+/* Address of key/value row t of sequence b, kv head g; NULL if the page id is bad. */
+static const float *kv_row(const problem *p, const float *pool, int b, int g, int64_t t) {
+    int32_t page = p->table[(int64_t)b * p->max_pages + t / p->P];
+    if (page < 0 || page >= p->num_pages) return NULL;
+    return pool + (((int64_t)page * p->Hkv + g) * p->P + t % p->P) * p->D;
+}
+
+static double score(const problem *p, const float *qrow, const float *krow) {
+    double acc = 0.0;
+    for (int d = 0; d < p->D; ++d) acc += (double)qrow[d] * (double)krow[d];
+    return p->scale * acc;
+}
+
+/*
+ * Full-KV attention, the plain definition.  rows == NULL computes every row into
+ * out[(b*Hq+h)*q_len+i][D]; otherwise rows[0..n_rows) lists flat row indices and
+ * out[j][D] receives row rows[j].  lse (may be NULL) gets one value per row.
+ */
+int oracle_attn(const float *q, const float *k_pages, const float *v_pages,
+                const int32_t *page_table, const int32_t *seq_lens,
+                int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
+                int q_len, double scale, const int64_t *rows, int64_t n_rows,
+                double *out, double *lse) {
+    problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
+                 max_pages, num_pages, q_len, scale};
+    if (check_problem(&p)) return 1;
+    int64_t total = rows ? n_rows : (int64_t)B * Hq * q_len;
+    int G = Hq / Hkv;
+    int err = 0;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < total; ++j) {
+        int64_t r = rows ? rows[j] : j;
+        int b, h, i;
+        if (r < 0 || r >= (int64_t)B * Hq * q_len) {
+#pragma omp atomic write
+            err = 1;
+            continue;
+        }
+        row_parts(&p, r, &b, &h, &i);
+        int g = h / G;
+        int64_t n = visible_keys(&p, b, i);
+        if (n < 0) {
+#pragma omp atomic write
+            err = 2;
+            continue;
+        }
+        const float *qrow = q + r * D;
+        double *s = (double *)malloc((size_t)n * sizeof(double));
+        if (!s) {
+#pragma omp atomic write
+            err = 4;
+            continue;
+        }
+        /* scores and their maximum */
+        double M = -INFINITY;
+        int bad = 0;
+        for (int64_t t = 0; t < n; ++t) {
+            const float *krow = kv_row(&p, k_pages, b, g, t);
+            if (!krow) { bad = 1; break; }
+            s[t] = score(&p, qrow, krow);
+            if (s[t] > M) M = s[t];
+        }
+        if (bad) {
+            free(s);
+#pragma omp atomic write
+            err = 3;
+            continue;
+        }
+        /* softmax weights and the weighted sum of value rows */
+        double l = 0.0;
+        double *o = out + j * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            double w = exp(s[t] - M);
+            l += w;
+            const float *vrow = kv_row(&p, v_pages, b, g, t);
+            for (int d = 0; d < D; ++d) o[d] += w * (double)vrow[d];
+        }
+        for (int d = 0; d < D; ++d) o[d] /= l;
+        if (lse) lse[j] = M + log(l);
+        free(s);
+    }
+    return err;
+}
+
+/*
+ * The page-by-page fold: each page's keys update the running state
+ *   m' = max(m, max_t s_t),  c = exp(m - m'),
+ *   l' = c l + sum_t exp(s_t - m'),  acc' = c acc + sum_t exp(s_t - m') v_t
+ * in logical page order; o = acc / l at the end.  Same argument convention as
+ * oracle_attn.  Used only to check the fold against the full-KV definition.
+ */
+int oracle_folded(const float *q, const float *k_pages, const float *v_pages,
+                  const int32_t *page_table, const int32_t *seq_lens,
+                  int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
+                  int q_len, double scale, const int64_t *rows, int64_t n_rows,
+                  double *out, double *lse) {
+    problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
+                 max_pages, num_pages, q_len, scale};
+    if (check_problem(&p)) return 1;
+    int64_t total = rows ? n_rows : (int64_t)B * Hq * q_len;
+    int G = Hq / Hkv;
+    int err = 0;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < total; ++j) {
+        int64_t r = rows ? rows[j] : j;
+        int b, h, i;
+        if (r < 0 || r >= (int64_t)B * Hq * q_len) {
+#pragma omp atomic write
+            err = 1;
+            continue;
+        }
+        row_parts(&p, r, &b, &h, &i);
+        int g = h / G;
+        int64_t n = visible_keys(&p, b, i);
+        if (n < 0) {
+#pragma omp atomic write
+            err = 2;
+            continue;
+        }
+        const float *qrow = q + r * D;
+        double *acc = out + j * D;
+        double *s = (double *)malloc((size_t)P * sizeof(double));
+        if (!s) {
+#pragma omp atomic write
+            err = 4;
+            continue;
+        }
+        for (int d = 0; d < D; ++d) acc[d] = 0.0;
+        double m = -INFINITY, l = 0.0;
+        int bad = 0;
+        for (int64_t t0 = 0; t0 < n && !bad; t0 += P) {
+            int64_t cnt = n - t0 < P ? n - t0 : P;
+            double m_page = -INFINITY;
+            for (int64_t u = 0; u < cnt; ++u) {
+                const float *krow = kv_row(&p, k_pages, b, g, t0 + u);
+                if (!krow) { bad = 1; break; }
+                s[u] = score(&p, qrow, krow);
+                if (s[u] > m_page) m_page = s[u];
+            }
+            if (bad) break;
+            double m_new = m_page > m ? m_page : m;
+            double c = exp(m - m_new); /* exp(-inf) = 0 on the first page */
+            l *= c;
+            for (int d = 0; d < D; ++d) acc[d] *= c;
+            for (int64_t u = 0; u < cnt; ++u) {
+                double w = exp(s[u] - m_new);
+                const float *vrow = kv_row(&p, v_pages, b, g, t0 + u);
+                l += w;
+                for (int d = 0; d < D; ++d) acc[d] += w * (double)vrow[d];
+            }
+            m = m_new;
+        }
+        free(s);
+        if (bad) {
+#pragma omp atomic write
+            err = 3;
+            continue;
+        }
+        for (int d = 0; d < D; ++d) acc[d] /= l;
+        if (lse) lse[j] = m + log(l);
+    }
+    return err;
+}
+
+/*
+ * Unnormalised softmax state of one row over the visible keys in
+ * [t_begin, t_end): m = max s_t, l = sum exp(s_t - m), acc = sum exp(s_t - m) v_t.
+ * An empty range gives m = -inf, l = 0, acc = 0.  One row per call (flat index r).
+ */
+int oracle_state(const float *q, const float *k_pages, const float *v_pages,
+                 const int32_t *page_table, const int32_t *seq_lens,
+                 int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
+                 int q_len, double scale, int64_t r, int64_t t_begin, int64_t t_end,
+                 double *m_out, double *l_out, double *acc) {
+    problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
+                 max_pages, num_pages, q_len, scale};
+    if (check_problem(&p)) return 1;
+    if (r < 0 || r >= (int64_t)B * Hq * q_len) return 1;
+    int b, h, i;
+    row_parts(&p, r, &b, &h, &i);
+    int g = h / (Hq / Hkv);
+    int64_t n = visible_keys(&p, b, i);
+    if (n < 0) return 2;
+    if (t_begin < 0) t_begin = 0;
+    if (t_end > n) t_end = n;
+    const float *qrow = q + r * D;
+    double m = -INFINITY;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        const float *krow = kv_row(&p, k_pages, b, g, t);
+        if (!krow) return 3;
+        double s = score(&p, qrow, krow);
+        if (s > m) m = s;
+    }
+    double l = 0.0;
+    for (int d = 0; d < D; ++d) acc[d] = 0.0;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        double w = exp(score(&p, qrow, kv_row(&p, k_pages, b, g, t)) - m);
+        const float *vrow = kv_row(&p, v_pages, b, g, t);
+        l += w;
+        for (int d = 0; d < D; ++d) acc[d] += w * (double)vrow[d];
+    }
+    *m_out = m;
+    *l_out = l;
+    return 0;
+}
+
+/*
+ * Structured merge of S partial states of one row:
+ *   M = max_s m_s,  l = sum_s exp(m_s - M) l_s,  o = sum_s exp(m_s - M) acc_s / l,
+ *   lse = M + log(l).  States with l_s == 0 (empty ranges) contribute nothing.
+ */
+int oracle_merge(int S, int D, const double *m, const double *l, const double *acc,
+                 double *out, double *lse) {
+    double M = -INFINITY;
+    for (int s = 0; s < S; ++s)
+        if (l[s] > 0.0 && m[s] > M) M = m[s];
+    if (M == -INFINITY) return 2;
+    double L = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int s = 0; s < S; ++s) {
+        if (l[s] <= 0.0) continue;
+        double w = exp(m[s] - M);
+        L += w * l[s];
+        for (int d = 0; d < D; ++d) out[d] += w * acc[(int64_t)s * D + d];
+    }
+    for (int d = 0; d < D; ++d) out[d] /= L;
+    if (lse) *lse = M + log(L);
+    return 0;
+}

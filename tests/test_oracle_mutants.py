@@ -1,0 +1,49 @@
+"""The pins must be strong enough to catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/oracle_attn.c (on the CPU), builds
+it, and runs the pin suite against it: the suite must fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle_attn.c")
+
+MUTANTS = {
+    "causal_off_by_one": ("int64_t n = L - p->q_len + i + 1;", "int64_t n = L - p->q_len + i;"),
+    "causal_reversed": ("int64_t n = L - p->q_len + i + 1;", "int64_t n = L - i;"),
+    "slot_index": ("* p->P + t % p->P) * p->D;", "* p->P + (t + 1) % p->P) * p->D;"),
+    "pool_transposed": ("(((int64_t)page * p->Hkv + g) * p->P", "(((int64_t)g * p->num_pages + page) * p->P"),
+    "page_index": ("p->table[(int64_t)b * p->max_pages + t / p->P]", "p->table[(int64_t)b * p->max_pages + t % p->max_pages]"),
+    "dot_operand": ("(double)qrow[d] * (double)krow[d]", "(double)qrow[d] * (double)krow[0]"),
+    "scale_dropped": ("return p->scale * acc;", "return acc;"),
+    "exp_sign": ("double w = exp(s[t] - M);", "double w = exp(M - s[t]);"),
+    "normalise_dropped": ("for (int d = 0; d < D; ++d) o[d] /= l;", ""),
+    "gqa_interleaved": ("int g = h / G;\n        int64_t n = visible_keys(&p, b, i);\n        if (n < 0) {\n#pragma omp atomic write\n            err = 2;\n            continue;\n        }\n        const float *qrow = q + r * D;\n        double *s = (double *)malloc",
+                        "int g = h % p.Hkv;\n        int64_t n = visible_keys(&p, b, i);\n        if (n < 0) {\n#pragma omp atomic write\n            err = 2;\n            continue;\n        }\n        const float *qrow = q + r * D;\n        double *s = (double *)malloc"),
+    "fold_rescale_dropped": ("l *= c;", ""),
+    "fold_rescale_sign": ("double c = exp(m - m_new);", "double c = exp(m_new - m);"),
+    "merge_weight_dropped": ("L += w * l[s];", "L += l[s];"),
+    "lse_shift_dropped": ("if (lse) lse[j] = M + log(l);", "if (lse) lse[j] = log(l);"),
+    "row_head_index": ("*h = (int)((r / p->q_len) % p->Hq);", "*h = (int)(r % p->Hq);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    orig, mutated = MUTANTS[name]
+    src = open(SRC).read()
+    assert orig in src, f"mutation site for {name} not found"
+    bad_src = tmp_path / "oracle_attn.c"
+    bad_src.write_text(src.replace(orig, mutated, 1))
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                           str(bad_src), "-o", str(lib), "-lm"])
+    env = dict(os.environ, ATLAS_ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
+    res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                          os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                         cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode != 0, f"mutant {name} passed every pin:\n{res.stdout[-2000:]}"
