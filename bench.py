@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark: paged causal GQA attention on GB300, one JSON line on stdout.
+
+Default workload (N=1): GQA decode -- batch 32, 32 q heads / 8 kv heads,
+head_dim 128, per-sequence context uniform on [1024, 32768] (seeded), 16-token
+pages in a shared shuffled pool, bf16 q/K/V, bf16 output.  A step is one call
+of atlas_attn_decode: split-KV fold of every page (page-table gather, scores,
+online softmax, PV, partial write) plus the log-sum-exp merge.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+  python bench.py --impl reference   # the fp64 CPU oracle on host cores
+
+Under torchrun each rank runs its own seeded batch on its own GPU (weak scaling,
+no collective on the data path); rank 0 prints the line, timing is the max over
+ranks.  KV bytes are algorithmic: every visible key's K and V row read once.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "decode KV GB/s (% of HBM peak); prefill TFLOP/s (% of bf16 TC peak)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["atlas", "reference"], default="atlas")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            data = json.load(f)
+        return data, "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+def work_of(prob):
+    """Algorithmic work of one call: (KV bytes, FLOPs)."""
+    kv = prob.kv_bytes()
+    lens = prob.seq_lens.to(torch.int64).cpu()
+    sq = prob.q_len
+    # keys seen by query rows: sum_b sum_i (L_b - sq + i + 1)
+    keys = int((lens * sq).sum()) - sq * (sq - 1) // 2 * prob.batch
+    flops = 4 * prob.head_dim * prob.n_q_heads * keys
+    return kv, flops
+
+
+def traffic_record(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
+    kernel source is unchanged since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    src = os.path.join(ROOT, "exact_causal_gqa_gb300", "csrc", "split_kv.cu")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if parts.get("kernel") == kernel and parts.get("workload") == workload and \
+                parts.get("source_sha") == sha:
+            return float(parts["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_atlas(args, world, rank, local):
+    import exact_causal_gqa_gb300 as atlas
+    from exact_causal_gqa_gb300 import inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    atlas.load_library()
+    cfg = inputs.CONFIGS[args.config]
+    seed = args.config + 1000 * rank
+    prob = inputs.make_config(args.config, seed=seed, device=dev)
+    kv_bytes, flops = work_of(prob)
+    out_dtype = torch.bfloat16 if prob.out_dtype == "bf16" else torch.float32
+    out = torch.empty(prob.q.shape, dtype=out_dtype, device=dev)
+    ws_bytes = atlas.workspace_size(prob.kind, prob.q.shape, prob.n_q_heads, prob.n_kv_heads,
+                                    prob.head_dim, prob.page_tokens, prob.max_pages,
+                                    prob.num_pages, dtype=prob.q.dtype, out_dtype=out_dtype,
+                                    split_tokens=args.split_tokens)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    timers = [atlas.EventTimer() for _ in range(args.steps)]
+    needs_flush = kv_bytes < 2 * L2_BYTES
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if needs_flush else None
+
+    def step(timer=None):
+        atlas.run(prob, out=out, workspace=ws, status=status, split_tokens=args.split_tokens,
+                  events=None if timer is None else timer.handles)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+
+    step_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    step_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            if flush is not None:
+                flush.fill_(float(k))  # evict the previous step's inputs from L2
+            step_start[k].record()
+            step(timers[k])
+            step_end[k].record()
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(step_start, step_end)]
+    main_ms = [t.main_ms() for t in timers]
+    ms = sum(step_ms) / len(step_ms)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    status_val = int(status.item())
+
+    # ---- end to end: pinned host inputs -> device -> kernels -> host output
+    e2e = None
+    if not args.no_e2e:
+        host = [t.to("cpu").pin_memory() for t in (prob.q, prob.k_pages, prob.v_pages,
+                                                    prob.page_table, prob.seq_lens)]
+        dbuf = [torch.empty_like(t, device=dev) for t in host]
+        host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        bi = sum(t.numel() * t.element_size() for t in host)
+        bo = host_out.numel() * host_out.element_size()
+
+        def e2e_step():
+            for d, h in zip(dbuf, host):
+                d.copy_(h, non_blocking=True)
+            atlas._call(prob.kind, *dbuf, prob.n_q_heads, prob.n_kv_heads, prob.head_dim,
+                        prob.page_tokens, prob.scale, out=out, workspace=ws, status=status,
+                        split_tokens=args.split_tokens)
+            host_out.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e_steps = max(3, min(args.steps, 10))
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        for _ in range(e_steps):
+            e2e_step()
+        ev1.record()
+        torch.cuda.synchronize(dev)
+        e_ms = torch.tensor([ev0.elapsed_time(ev1) / e_steps], dtype=torch.float64, device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(e_ms, op=torch.distributed.ReduceOp.MAX)
+        e2e = (float(e_ms.item()), bi, bo)
+
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    decode_like = prob.kind != "prefill"
+    main_avg = sum(main_ms) / len(main_ms)
+    if decode_like:
+        value = world * kv_bytes / (ms_max * 1e-3) / 1e9
+        unit = "GB/s"
+        achieved = kv_bytes / (main_avg * 1e-3) / 1e9
+        peak = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
+        bound = "hbm"
+    else:
+        value = world * flops / (ms_max * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        achieved = flops / (main_avg * 1e-3) / 1e12
+        peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+        bound = "tensor"
+    kernel = "split_bf16_kernel" if prob.dtype == "bf16" else "split_f32_kernel"
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": unit,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": prob.dtype,
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
+        "config": {
+            "workload": cfg["name"],
+            "kind": prob.kind, "batch": prob.batch, "n_q_heads": prob.n_q_heads,
+            "n_kv_heads": prob.n_kv_heads, "head_dim": prob.head_dim,
+            "page_tokens": prob.page_tokens, "q_len": prob.q_len,
+            "context": list(cfg["ctx"]), "sum_context": int(prob.seq_lens.sum()),
+            "kv_bytes_per_step": kv_bytes, "flops_per_step": flops,
+            "l2": ("flushed between steps (2x L2 write)" if flush is not None
+                   else f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB KV vs 129 MB)"),
+            "parallelism": f"replicas x{world} (independent batches per GPU)",
+            "split_tokens": args.split_tokens or "auto",
+            "per_step_ms": {"min": round(min(step_ms), 5),
+                            "median": round(statistics.median(step_ms), 5)},
+            "main_kernel_ms": round(main_avg, 5),
+            "wall_s": round(wall, 4),
+        },
+        "roofline": {
+            "kernel": kernel,
+            "bound": bound,
+            "achieved": round(achieved, 3),
+            "peak": peak,
+            "peak_source": pk_kind,
+            "unit": unit,
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic_record(kernel, cfg["name"]),
+        },
+        "gpu_launches": 2 * args.steps,
+        "device_status": status_val,
+    }
+    clk = clocks.summary()
+    line["clocks"] = clk
+    if e2e is not None:
+        e_ms, bi, bo = e2e
+        e_val = (world * kv_bytes / (e_ms * 1e-3) / 1e9) if decode_like else \
+            (world * flops / (e_ms * 1e-3) / 1e12)
+        line["e2e"] = {"value": round(e_val, 3), "unit": unit, "ms_per_step": round(e_ms, 4),
+                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    line["cpu_baseline"] = cpu_baseline(args.config, prob, decode_like)
+    return line
+
+
+def oracle_sample(index, prob_host, decode_like, budget_s):
+    """Time the fp64 oracle on whole (sequence, kv head) groups of the workload
+    until about budget_s of CPU work; returns (value, unit, cores, sample)."""
+    import numpy as np
+    import oracle
+    q = prob_host.q.float().numpy()
+    k = prob_host.k_pages.float().numpy()
+    v = prob_host.v_pages.float().numpy()
+    table = prob_host.page_table.numpy()
+    lens = prob_host.seq_lens.numpy()
+    G = prob_host.n_q_heads // prob_host.n_kv_heads
+    rng = np.random.default_rng(12345)
+    groups = [(b, g) for b in range(prob_host.batch) for g in range(prob_host.n_kv_heads)]
+    order = rng.permutation(len(groups))
+    done_bytes, done_flops, elapsed, n_groups = 0, 0, 0.0, 0
+    for gi in order:
+        b, g = groups[gi]
+        rows = [((b * prob_host.n_q_heads + g * G + j) * prob_host.q_len + i)
+                for j in range(G) for i in range(prob_host.q_len)]
+        # bound the rows of very long query blocks (prefill): take a spread of them
+        if len(rows) > 512:
+            rows = rows[:: max(1, len(rows) // 512)]
+        t0 = time.perf_counter()
+        oracle.attn(q, k, v, table, lens, prob_host.n_q_heads, prob_host.n_kv_heads,
+                    prob_host.scale, rows=np.asarray(rows))
+        elapsed += time.perf_counter() - t0
+        L = int(lens[b])
+        done_bytes += 2 * L * prob_host.head_dim * prob_host.k_pages.element_size()
+        for r in rows:
+            i = r % prob_host.q_len
+            done_flops += 4 * prob_host.head_dim * (L - prob_host.q_len + i + 1)
+        n_groups += 1
+        if elapsed >= budget_s:
+            break
+    if decode_like:
+        value, unit = done_bytes / elapsed / 1e9, "GB/s"
+    else:
+        value, unit = done_flops / elapsed / 1e12, "TFLOP/s"
+    sample = (f"{n_groups} of {len(groups)} (sequence, kv head) groups, all their query rows "
+              f"(prefill: up to 512 rows per group), {elapsed:.1f} s of oracle time")
+    return value, unit, oracle.num_threads(), sample
+
+
+def cpu_baseline(index, prob, decode_like, budget_s=12.0):
+    try:
+        host = prob.to("cpu")
+        value, unit, cores, sample = oracle_sample(index, host, decode_like, budget_s)
+        return {"value": round(value, 4), "unit": unit, "cores": cores, "kind": "oracle",
+                "sample": sample}
+    except Exception as exc:  # the baseline is reported, never fatal
+        return {"value": None, "unit": None, "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"failed: {exc}"}
+
+
+def run_reference(args, world, rank):
+    from exact_causal_gqa_gb300 import inputs
+    if rank != 0:
+        return None
+    cfg = inputs.CONFIGS[args.config]
+    prob = inputs.make_config(args.config, device="cpu")
+    decode_like = prob.kind != "prefill"
+    warm = max(3, args.warmup)
+    per_step = max(0.5, 120.0 / (args.steps + warm))
+    vals = []
+    t_all = time.perf_counter()
+    for k in range(warm + args.steps):
+        value, unit, cores, sample = oracle_sample(args.config, prob, decode_like, per_step)
+        if k >= warm:
+            vals.append(value)
+    wall = time.perf_counter() - t_all
+    value = statistics.median(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": warm,
+        "ms_per_step": round(wall * 1e3 / (warm + args.steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
+        "config": {"workload": cfg["name"], "kind": prob.kind},
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        if world > 1:
+            torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+        line = run_atlas(args, world, rank, local)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

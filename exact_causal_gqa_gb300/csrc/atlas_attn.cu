@@ -1,0 +1,253 @@
+// atlas_attn.cu -- the C ABI: argument checks, the split plan, tensor-map
+// encoding and kernel launches.  Declared in include/atlas_attn.h.
+#include "internal.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <limits.h>
+#include <stdint.h>
+#include <mutex>
+
+namespace atlas {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult res;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &res) == cudaSuccess &&
+            res == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// CTAs the automatic split plan aims for at the largest context the page table
+// allows: 152 SMs x 2 resident CTAs x 8 waves.  A pure function of the call's
+// sizes, so a given problem always gets the same split (and the same bits).
+constexpr int64_t kPlanCtas = 152 * 2 * 8;
+
+enum class Path { SplitBF16, SplitF32 };
+
+struct Plan {
+    Path path;
+    int chunk, n_chunks, col_tiles, G;
+    size_t acc_bytes, ml_offset, ws_bytes;
+};
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int32_t P,
+                       const atlas_launch *L, Plan *plan) {
+    if (!L) return ATLAS_ERR_INVALID_ARG;
+    if (kind != ATLAS_KIND_DECODE && kind != ATLAS_KIND_SUFFIX && kind != ATLAS_KIND_PREFILL)
+        return ATLAS_ERR_INVALID_ARG;
+    if (L->batch < 1 || L->max_pages_per_seq < 1 || L->num_pages < 1 || L->q_len < 1 || Hq < 1 ||
+        Hkv < 1 || Hq % Hkv != 0)
+        return ATLAS_ERR_INVALID_ARG;
+    if (kind == ATLAS_KIND_DECODE && L->q_len != 1) return ATLAS_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return ATLAS_ERR_UNSUPPORTED;
+    if (!is_pow2(P) || P < 8 || P > 128) return ATLAS_ERR_UNSUPPORTED;
+    if (L->q_dtype != L->kv_dtype) return ATLAS_ERR_UNSUPPORTED;
+    if (L->kv_dtype == ATLAS_F32) {
+        if (L->out_dtype != ATLAS_F32) return ATLAS_ERR_UNSUPPORTED;
+    } else if (L->kv_dtype == ATLAS_BF16) {
+        if (L->out_dtype != ATLAS_F32 && L->out_dtype != ATLAS_BF16) return ATLAS_ERR_UNSUPPORTED;
+    } else {
+        return ATLAS_ERR_UNSUPPORTED;
+    }
+    const int64_t max_ctx = (int64_t)L->max_pages_per_seq * P;
+    if (max_ctx > INT32_MAX / 2) return ATLAS_ERR_INVALID_ARG;
+    if ((int64_t)L->num_pages * Hkv * P >= INT32_MAX) return ATLAS_ERR_INVALID_ARG;
+    if (L->q_len > max_ctx) return ATLAS_ERR_INVALID_ARG;
+    if (L->split_tokens < 0 || L->split_tokens % kSplitBlockTokens != 0)
+        return ATLAS_ERR_INVALID_ARG;
+
+    const int G = Hq / Hkv;
+    plan->G = G;
+    plan->path = L->kv_dtype == ATLAS_BF16 ? Path::SplitBF16 : Path::SplitF32;
+    const int cols = plan->path == Path::SplitBF16 ? split_bf16_cols_per_cta(G, L->q_len) : 8;
+    plan->col_tiles = (G * L->q_len + cols - 1) / cols;
+    if ((int64_t)Hkv * plan->col_tiles > 65535 || L->batch > 65535) return ATLAS_ERR_UNSUPPORTED;
+
+    int64_t chunk = L->split_tokens;
+    if (chunk == 0) {
+        const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
+        chunk = round_up((max_ctx * units + kPlanCtas - 1) / kPlanCtas, kSplitBlockTokens);
+        if (chunk < 512) chunk = 512;
+        if (chunk > 8192) chunk = 8192;
+    }
+    if (chunk > max_ctx) chunk = round_up(max_ctx, kSplitBlockTokens);
+    plan->chunk = (int)chunk;
+    plan->n_chunks = (int)((max_ctx + chunk - 1) / chunk);
+
+    const int64_t rows = (int64_t)L->batch * Hq * L->q_len;
+    plan->acc_bytes = (size_t)rows * plan->n_chunks * D * sizeof(float);
+    plan->ml_offset = (size_t)round_up((int64_t)plan->acc_bytes, 256);
+    plan->ws_bytes = plan->ml_offset + (size_t)rows * plan->n_chunks * 2 * sizeof(float);
+    return ATLAS_OK;
+}
+
+// 2-D view of a page pool: rows = num_pages*Hkv*P, D bf16 per row; boxes of
+// 64 elements x min(P, 64) rows with 128-byte swizzling.
+atlas_status encode_pool_map(CUtensorMap *map, const void *pool, int32_t num_pages, int32_t Hkv,
+                             int32_t P, int32_t D) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return ATLAS_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_pages * Hkv * P};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)(P < kSplitBlockTokens ? P : kSplitBlockTokens)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATLAS_OK : ATLAS_ERR_CUDA;
+}
+
+atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void *v_pages,
+                 const int32_t *page_table, const int32_t *seq_lens, int32_t Hq, int32_t Hkv,
+                 int32_t D, int32_t P, float scale, const atlas_launch *L) {
+    if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !L || !L->out)
+        return ATLAS_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(L->out) ||
+        !aligned16(L->workspace))
+        return ATLAS_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return ATLAS_ERR_INVALID_ARG;
+    Plan plan;
+    atlas_status st = make_plan(kind, Hq, Hkv, D, P, L, &plan);
+    if (st != ATLAS_OK) return st;
+    if (plan.ws_bytes > 0 && (!L->workspace || L->workspace_bytes < plan.ws_bytes))
+        return ATLAS_ERR_WORKSPACE;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(L->stream);
+    // A sticky error from earlier work is not ours to report as a launch failure,
+    // but a pending non-sticky one would be picked up by our launch check.
+    (void)cudaGetLastError();
+
+    SplitParams sp{};
+    sp.q = q;
+    sp.k_pages = k_pages;
+    sp.v_pages = v_pages;
+    sp.page_table = page_table;
+    sp.seq_lens = seq_lens;
+    sp.B = L->batch;
+    sp.Hq = Hq;
+    sp.Hkv = Hkv;
+    sp.G = plan.G;
+    sp.D = D;
+    sp.P = P;
+    sp.q_len = L->q_len;
+    sp.max_pages = L->max_pages_per_seq;
+    sp.num_pages = L->num_pages;
+    sp.chunk = plan.chunk;
+    sp.n_chunks = plan.n_chunks;
+    sp.col_tiles = plan.col_tiles;
+    sp.require_full = kind == ATLAS_KIND_PREFILL;
+    sp.scale_log2 = scale * kLog2e;
+    sp.ws_acc = static_cast<float *>(L->workspace);
+    sp.ws_ml = reinterpret_cast<float *>(static_cast<char *>(L->workspace) + plan.ml_offset);
+    sp.status = L->status_word;
+    sp.debug_flags = L->debug_flags;
+
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    if (L->events)
+        for (int i = 0; i < 3; ++i) ev[i] = static_cast<cudaEvent_t>(L->events[i]);
+    cudaError_t err;
+    if (ev[0] && cudaEventRecord(ev[0], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+    if (plan.path == Path::SplitBF16) {
+        CUtensorMap tmK, tmV;
+        st = encode_pool_map(&tmK, k_pages, L->num_pages, Hkv, P, D);
+        if (st == ATLAS_OK) st = encode_pool_map(&tmV, v_pages, L->num_pages, Hkv, P, D);
+        if (st != ATLAS_OK) return st;
+        err = launch_split_bf16(sp, tmK, tmV, stream);
+    } else {
+        err = launch_split_f32(sp, stream);
+    }
+    if (err != cudaSuccess) return ATLAS_ERR_CUDA;
+    if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+
+    MergeParams mp{};
+    mp.seq_lens = seq_lens;
+    mp.B = L->batch;
+    mp.Hq = Hq;
+    mp.D = D;
+    mp.q_len = L->q_len;
+    mp.max_pages = L->max_pages_per_seq;
+    mp.P = P;
+    mp.chunk = plan.chunk;
+    mp.n_chunks = plan.n_chunks;
+    mp.require_full = sp.require_full;
+    mp.ws_acc = sp.ws_acc;
+    mp.ws_ml = sp.ws_ml;
+    mp.out = L->out;
+    mp.out_bf16 = L->out_dtype == ATLAS_BF16;
+    mp.lse = L->lse;
+    err = launch_merge(mp, stream);
+    if (err != cudaSuccess) return ATLAS_ERR_CUDA;
+    if (ev[2] && cudaEventRecord(ev[2], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+    return ATLAS_OK;
+}
+
+}  // namespace
+}  // namespace atlas
+
+extern "C" {
+
+atlas_status atlas_attn_decode(const void *q, const void *k_pages, const void *v_pages,
+                               const int32_t *page_table, const int32_t *seq_lens,
+                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                               int32_t page_tokens, float scale, const atlas_launch *L) {
+    return atlas::run(ATLAS_KIND_DECODE, q, k_pages, v_pages, page_table, seq_lens, n_q_heads,
+                      n_kv_heads, head_dim, page_tokens, scale, L);
+}
+
+atlas_status atlas_attn_suffix(const void *q, const void *k_pages, const void *v_pages,
+                               const int32_t *page_table, const int32_t *seq_lens,
+                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                               int32_t page_tokens, float scale, const atlas_launch *L) {
+    return atlas::run(ATLAS_KIND_SUFFIX, q, k_pages, v_pages, page_table, seq_lens, n_q_heads,
+                      n_kv_heads, head_dim, page_tokens, scale, L);
+}
+
+atlas_status atlas_attn_prefill(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *page_table, const int32_t *seq_lens,
+                                int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                int32_t page_tokens, float scale, const atlas_launch *L) {
+    return atlas::run(ATLAS_KIND_PREFILL, q, k_pages, v_pages, page_table, seq_lens, n_q_heads,
+                      n_kv_heads, head_dim, page_tokens, scale, L);
+}
+
+size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,
+                                 int32_t head_dim, int32_t page_tokens, const atlas_launch *L) {
+    atlas::Plan plan;
+    if (atlas::make_plan(kind, n_q_heads, n_kv_heads, head_dim, page_tokens, L, &plan) != ATLAS_OK)
+        return SIZE_MAX;
+    return plan.ws_bytes;
+}
+
+const char *atlas_attn_status_string(atlas_status status) {
+    switch (status) {
+        case ATLAS_OK: return "ok";
+        case ATLAS_ERR_INVALID_ARG: return "invalid argument";
+        case ATLAS_ERR_UNSUPPORTED: return "unsupported head_dim, page_tokens or dtype";
+        case ATLAS_ERR_WORKSPACE: return "workspace missing or too small";
+        case ATLAS_ERR_CUDA: return "CUDA runtime or driver call failed";
+        case ATLAS_ERR_DEVICE: return "a kernel reported a device-side error";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// internal.h -- parameter blocks and launchers shared by the host entry points
+// (atlas_attn.cu) and the kernel translation units.  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "atlas_attn.h"
+
+namespace atlas {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// A bounded wait gives up after this long and reports ATLAS_DEV_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Keys per pipeline stage of the split-KV kernels.
+constexpr int kSplitBlockTokens = 64;
+
+// Everything the split-KV kernels (bf16 mma.sync and f32) and the merge need.
+// "Columns" are the query rows one (sequence, kv head) owns: column n is q head
+// g = n / q_len of the group and query row i = n % q_len.
+struct SplitParams {
+    const void *q;              // [B][Hq][q_len][D]
+    const void *k_pages;        // f32 path reads the pools directly
+    const void *v_pages;
+    const int32_t *page_table;  // [B][max_pages]
+    const int32_t *seq_lens;    // [B]
+    int32_t B, Hq, Hkv, G, D, P, q_len, max_pages, num_pages;
+    int32_t chunk;              // keys per split (multiple of 64)
+    int32_t n_chunks;           // splits per (sequence, kv head): ceil(max_pages*P / chunk)
+    int32_t col_tiles;          // ceil(G*q_len / columns per CTA)
+    int32_t require_full;       // prefill: seq_len must equal q_len
+    float scale_log2;           // scale * log2(e)
+    float *ws_acc;              // [B*Hq*q_len][n_chunks][D]   unnormalised accumulators
+    float *ws_ml;               // [B*Hq*q_len][n_chunks][2]   (m in log2 units, l)
+    uint32_t *status;           // may be null
+    uint32_t debug_flags;
+};
+
+struct MergeParams {
+    const int32_t *seq_lens;
+    int32_t B, Hq, D, q_len, max_pages, P, chunk, n_chunks, require_full;
+    const float *ws_acc;
+    const float *ws_ml;
+    void *out;
+    int32_t out_bf16;
+    float *lse;
+};
+
+// Columns handled by one CTA of the bf16 split kernel.
+int split_bf16_cols_per_cta(int G, int q_len);
+
+cudaError_t launch_split_bf16(const SplitParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                              cudaStream_t stream);
+cudaError_t launch_split_f32(const SplitParams &p, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
+
+}  // namespace atlas

@@ -1,0 +1,110 @@
+// merge.cu -- structured log-sum-exp merge of split-KV partial states
+// (CPUAttn README, "Operator model": split-K is offered only with a structured
+// merge).  For one output row with splits s = 0..S-1 holding (m_s, l_s, acc_s),
+// m in log2 units:
+//   M = max_s m_s,  w_s = 2^(m_s - M),  o = sum_s w_s acc_s / sum_s w_s l_s,
+//   lse = ln 2 * (M + log2 sum_s w_s l_s).
+// One warp per row; lanes split the head dimension (float4 / float2 loads).
+// S is derived on the device from seq_lens, so no host sync is needed.
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <math.h>
+
+namespace atlas {
+namespace {
+
+constexpr int kRowsPerCta = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kRowsPerCta * 32) merge_kernel(const MergeParams p) {
+    constexpr int DPL = D / 32;
+    const int lane = threadIdx.x % 32;
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + threadIdx.x / 32;
+    const int64_t rows = (int64_t)p.B * p.Hq * p.q_len;
+    if (row >= rows) return;
+    const int i = (int)(row % p.q_len);
+    const int b = (int)(row / ((int64_t)p.Hq * p.q_len));
+    const int L = p.seq_lens[b];
+    const bool bad_len = L < p.q_len || L > p.max_pages * p.P || (p.require_full && L != p.q_len);
+
+    float o[DPL];
+    float lse = __int_as_float(0x7fc00000);
+    bool nan_row = bad_len;
+    if (!bad_len) {
+        const int visible = L - p.q_len + i + 1;
+        const int nsplit = (visible + p.chunk - 1) / p.chunk;
+        const float *ml = p.ws_ml + row * p.n_chunks * 2;
+        float M = -INFINITY;
+        bool has_nan = false;
+        for (int s = lane; s < nsplit; s += 32) {
+            const float m = ml[2 * s], l = ml[2 * s + 1];
+            if (isnan(l) || isnan(m)) has_nan = true;
+            else if (l > 0.f) M = fmaxf(M, m);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        has_nan = __any_sync(0xffffffffu, has_nan);
+        nan_row = has_nan || M == -INFINITY;
+        if (!nan_row) {
+            float acc[DPL];
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+            float lsum = 0.f;
+            const float *wa = p.ws_acc + row * p.n_chunks * D + lane * DPL;
+            for (int s = 0; s < nsplit; ++s) {
+                const float m = ml[2 * s], l = ml[2 * s + 1];
+                const float w = l > 0.f ? ex2(m - M) : 0.f;
+                lsum = fmaf(w, l, lsum);
+                if (DPL == 4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(wa + (int64_t)s * D);
+                    acc[0] = fmaf(w, a.x, acc[0]);
+                    acc[1] = fmaf(w, a.y, acc[1]);
+                    acc[2] = fmaf(w, a.z, acc[2]);
+                    acc[3] = fmaf(w, a.w, acc[3]);
+                } else {
+                    const float2 a = *reinterpret_cast<const float2 *>(wa + (int64_t)s * D);
+                    acc[0] = fmaf(w, a.x, acc[0]);
+                    acc[1] = fmaf(w, a.y, acc[1]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) o[j] = acc[j] / lsum;
+            lse = kLn2 * (M + log2f(lsum));
+        }
+    }
+    if (nan_row) {
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) o[j] = __int_as_float(0x7fc00000);
+        lse = __int_as_float(0x7fc00000);
+    }
+    const int64_t off = row * D + lane * DPL;
+    if (p.out_bf16) {
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + off;
+        if (DPL == 4) {
+            uint2 v;
+            v.x = pack_bf16(o[0], o[1]);
+            v.y = pack_bf16(o[2], o[3]);
+            *reinterpret_cast<uint2 *>(out) = v;
+        } else {
+            *reinterpret_cast<uint32_t *>(out) = pack_bf16(o[0], o[1]);
+        }
+    } else {
+        float *out = static_cast<float *>(p.out) + off;
+        if (DPL == 4) *reinterpret_cast<float4 *>(out) = make_float4(o[0], o[1], o[2], o[3]);
+        else *reinterpret_cast<float2 *>(out) = make_float2(o[0], o[1]);
+    }
+    if (p.lse && lane == 0) p.lse[row] = lse;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream) {
+    const int64_t rows = (int64_t)p.B * p.Hq * p.q_len;
+    const unsigned grid = (unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta);
+    if (p.D == 128) merge_kernel<128><<<grid, kRowsPerCta * 32, 0, stream>>>(p);
+    else merge_kernel<64><<<grid, kRowsPerCta * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace atlas

@@ -1,0 +1,530 @@
+// split_kv.cu -- split-KV attention over paged K/V for few query rows per
+// (sequence, kv head): decode (one row per q head) and short suffixes.
+//
+// Each CTA owns one (split of the key axis, kv head, sequence) and up to 8 or 16
+// "columns" (q head of the GQA group x query row).  It folds its pages into an
+// online-softmax state (m, l, acc) -- the page-by-page fold of the CFR-Atlas
+// README (opening paragraph, "Core contract") -- and writes that partial state;
+// merge.cu combines the splits (CPUAttn README, "Operator model": split-K only
+// with a structured merge).
+//
+// bf16 path, per CTA: one producer warp gathers the split's pages through the
+// page table with 2-D TMA loads (128-byte swizzle) into a STAGES-deep ring of
+// 64-key K/V blocks; four consumer warps each take 16 keys of every block and
+// run both contractions on mma.sync tensor-core tiles with the keys on M:
+//   S^T[16 keys x 8 cols]  = K[16 x D] . Q^T[D x 8]      (ldmatrix from the ring)
+//   O^T[D x 8 cols]       += V^T[D x 16] . P^T[16 x 8]    (ldmatrix.trans; P^T via movmatrix)
+// P is fed as bf16 hi + lo parts, so the PV product keeps ~16 bits of P.
+// Column max / sum reductions are quad shuffles.
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <math.h>
+
+namespace atlas {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
+constexpr int BT = kSplitBlockTokens;
+
+__device__ __forceinline__ void record(uint32_t *status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+__device__ __forceinline__ bool seq_len_bad(const SplitParams &p, int L) {
+    return L < p.q_len || L > p.max_pages * p.P || (p.require_full && L != p.q_len);
+}
+
+// Flat output row of column n of (b, hkv).
+__device__ __forceinline__ int64_t column_row(const SplitParams &p, int b, int hkv, int n) {
+    const int h = hkv * p.G + n / p.q_len;
+    const int i = n % p.q_len;
+    return ((int64_t)b * p.Hq + h) * p.q_len + i;
+}
+
+// Keys visible to column n (absolute count), as defined by the suffix rule.
+__device__ __forceinline__ int column_visible(const SplitParams &p, int L, int n) {
+    return L - p.q_len + (n % p.q_len) + 1;
+}
+
+// Shared prologue: decides whether this CTA has work.  Returns false when the
+// CTA must exit (nothing visible, or an error that has been recorded).
+template <int NCOLS>
+__device__ bool split_prologue(const SplitParams &p, int &L, int &kv_begin, int &kv_end,
+                               int &col0, int &ncols) {
+    const int b = blockIdx.z;
+    const int hkv = blockIdx.y / p.col_tiles;
+    const int ct = blockIdx.y % p.col_tiles;
+    L = p.seq_lens[b];
+    if (seq_len_bad(p, L)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) record(p.status, ATLAS_DEV_BAD_SEQLEN);
+        return false;  // the merge writes NaN rows for this sequence
+    }
+    col0 = ct * NCOLS;
+    ncols = min(NCOLS, p.G * p.q_len - col0);
+    int i_max = 0;
+    for (int c = 0; c < ncols; ++c) i_max = max(i_max, (col0 + c) % p.q_len);
+    const int kv_hi = L - p.q_len + i_max + 1;
+    kv_begin = blockIdx.x * p.chunk;
+    if (kv_begin >= kv_hi) return false;
+    kv_end = min(kv_hi, kv_begin + p.chunk);
+
+    // Every page id this split will touch must be inside the pool.
+    const int pg0 = kv_begin / p.P, pg1 = (kv_end - 1) / p.P;
+    bool bad = false;
+    for (int pg = pg0 + (int)threadIdx.x; pg <= pg1; pg += blockDim.x) {
+        const int id = p.page_table[(int64_t)b * p.max_pages + pg];
+        bad |= (id < 0 || id >= p.num_pages);
+    }
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0) record(p.status, ATLAS_DEV_BAD_PAGE);
+        for (int c = threadIdx.x; c < ncols; c += blockDim.x) {
+            float *ml = p.ws_ml + (column_row(p, b, hkv, col0 + c) * p.n_chunks + blockIdx.x) * 2;
+            ml[0] = __int_as_float(0x7fc00000);
+            ml[1] = __int_as_float(0x7fc00000);
+        }
+        return false;
+    }
+    return true;
+}
+
+// Combine the per-warp states held in shared memory and write this split's
+// partial (m, l, acc) for every valid column.  cm/cl: [W][NCOLS]; cacc: [W][NCOLS][D].
+template <int W, int NCOLS, int D>
+__device__ void write_partials(const SplitParams &p, const float *cm, const float *cl,
+                               const float *cacc, int col0, int ncols, bool failed) {
+    const int b = blockIdx.z;
+    const int hkv = blockIdx.y / p.col_tiles;
+    for (int idx = threadIdx.x; idx < NCOLS * D; idx += blockDim.x) {
+        const int c = idx / D, d = idx % D;
+        if (c >= ncols) continue;
+        const int64_t row = column_row(p, b, hkv, col0 + c);
+        const int64_t slot = row * p.n_chunks + blockIdx.x;
+        if (failed) {
+            if (d == 0) {
+                p.ws_ml[slot * 2] = __int_as_float(0x7fc00000);
+                p.ws_ml[slot * 2 + 1] = __int_as_float(0x7fc00000);
+            }
+            continue;
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, cm[w * NCOLS + c]);
+        float a = 0.f, l = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float f = ex2(cm[w * NCOLS + c] - M);
+                a += f * cacc[(w * NCOLS + c) * D + d];
+                l += f * cl[w * NCOLS + c];
+            }
+        }
+        p.ws_acc[slot * D + d] = a;
+        if (d == 0) {
+            p.ws_ml[slot * 2] = M;
+            p.ws_ml[slot * 2 + 1] = l;
+        }
+    }
+}
+
+template <int D, int NT, int STAGES>
+struct SplitLayout {
+    static constexpr int kTile = BT * D * 2;           // one 64-key K or V block, bf16
+    static constexpr int kStage = 2 * kTile;           // K then V
+    static constexpr int kBars = STAGES * kStage;      // full[STAGES], empty[STAGES]
+    static constexpr int kFlags = kBars + 2 * STAGES * 8;
+    static constexpr int kBytes = kFlags + 16 + 1024;  // + alignment slack
+    static constexpr int kCombine = kConsumerWarps * NT * 8 * (D + 2) * 4;
+    static_assert(kCombine <= kBars, "combine scratch must fit in the ring");
+};
+
+template <int D, int NT, int STAGES>
+__global__ void __launch_bounds__(kSplitThreads, 2)
+    split_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    using Lay = SplitLayout<D, NT, STAGES>;
+    constexpr int NCOLS = NT * 8;
+    constexpr int KSTEPS = D / 16;
+    constexpr int SLAB = BT * 128;  // bytes of one 64-element-wide slab of a block
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t full0 = sbase + Lay::kBars;
+    const uint32_t empty0 = full0 + STAGES * 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lay::kFlags);
+
+    int L, kv_begin, kv_end, col0, ncols;
+    if (!split_prologue<NCOLS>(p, L, kv_begin, kv_end, col0, ncols)) return;
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int b = blockIdx.z;
+    const int hkv = blockIdx.y / p.col_tiles;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int nblocks = (kv_end - kv_begin + BT - 1) / BT;
+    bool failed = false;
+
+    // Per-thread softmax state for columns nt*8 + 2*(lane%4) + {0,1}.
+    float m_run[NT][2], l_run[NT][2];
+    float acc[KSTEPS][NT][4];
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer warp
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            const uint64_t policy = policy_evict_first();
+            const int BR = p.P < BT ? p.P : BT;  // rows per box
+            const int subs = BT / BR;
+            int issued = 0;
+            for (int j = 0; j < nblocks; ++j) {
+                const int s = j % STAGES;
+                if (j >= STAGES &&
+                    !mbar_wait_bounded(empty0 + 8 * s, ((j / STAGES) - 1) & 1, abort_flag,
+                                       kWaitLimitNs)) {
+                    failed = true;
+                    break;
+                }
+                const int t0 = kv_begin + j * BT;
+                const int nsub = min(subs, (kv_end - t0 + BR - 1) / BR);
+                if ((p.debug_flags & ATLAS_DEBUG_WITHHOLD_STAGE) && j == 0) continue;
+                mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nsub * BR * D * 2 * 2));
+                const uint32_t kdst = sbase + s * Lay::kStage;
+                const uint32_t vdst = kdst + Lay::kTile;
+                for (int sb = 0; sb < nsub; ++sb) {
+                    const int t = t0 + sb * BR;
+                    const int phys = p.page_table[(int64_t)b * p.max_pages + t / p.P];
+                    const int y = (phys * p.Hkv + hkv) * p.P + (t % p.P);
+#pragma unroll
+                    for (int slab = 0; slab < D / 64; ++slab) {
+                        tma_load_2d_hint(kdst + slab * SLAB + sb * BR * 128, &tmK, slab * 64, y,
+                                         full0 + 8 * s, policy);
+                        tma_load_2d_hint(vdst + slab * SLAB + sb * BR * 128, &tmV, slab * 64, y,
+                                         full0 + 8 * s, policy);
+                    }
+                }
+                issued = j + 1;
+            }
+            if (failed) {
+                *abort_flag = 1;
+                // Let the copies already in flight land before the CTA exits.
+                int no_abort = 0;
+                for (int j = max(0, issued - STAGES); j < issued; ++j) {
+                    if ((p.debug_flags & ATLAS_DEBUG_WITHHOLD_STAGE) && j == 0) continue;
+                    mbar_wait_bounded(full0 + 8 * (j % STAGES), (j / STAGES) & 1,
+                                      (volatile int *)&no_abort, kWaitLimitNs);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ consumer warps
+        // Q^T as mma B fragments: element k = d, n = column lane/4.
+        uint32_t qf[KSTEPS][NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int c = nt * 8 + lane / 4;
+            const __nv_bfloat16 *qrow = nullptr;
+            if (c < ncols) qrow = static_cast<const __nv_bfloat16 *>(p.q) +
+                                   column_row(p, b, hkv, col0 + c) * D;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int d0 = kk * 16 + 2 * (lane % 4);
+                qf[kk][nt][0] = qrow ? *reinterpret_cast<const uint32_t *>(qrow + d0) : 0u;
+                qf[kk][nt][1] = qrow ? *reinterpret_cast<const uint32_t *>(qrow + d0 + 8) : 0u;
+            }
+        }
+        // Key limit of each of this thread's score columns (0 for padding columns).
+        int lim[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = nt * 8 + 2 * (lane % 4) + e;
+                lim[nt][e] = c < ncols ? min(kv_end, column_visible(p, L, col0 + c)) : 0;
+                m_run[nt][e] = -INFINITY;
+                l_run[nt][e] = 0.f;
+            }
+#pragma unroll
+        for (int dt = 0; dt < KSTEPS; ++dt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[dt][nt][e] = 0.f;
+
+        for (int j = 0; j < nblocks; ++j) {
+            const int s = j % STAGES;
+            // Warp-uniform decision: the mma.sync below needs every lane.
+            const bool landed = __all_sync(
+                0xffffffffu, mbar_wait_bounded(full0 + 8 * s, (j / STAGES) & 1, abort_flag,
+                                               kWaitLimitNs));
+            if (!landed) {
+                failed = true;
+                *abort_flag = 1;
+                break;
+            }
+            const int key0 = kv_begin + j * BT + 16 * warp;
+            const int valid = kv_end - key0;
+            if (valid > 0) {
+                const uint32_t kt = sbase + s * Lay::kStage;
+                const uint32_t vt = kt + Lay::kTile;
+                // ---- S^T = K . Q^T
+                float sc[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int r = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int d = kk * 16 + (lane >> 4) * 8;
+                    uint32_t a[4];
+                    ldmatrix_x4(kt + (d / 64) * SLAB + sw128(r, (d % 64) / 8), a[0], a[1], a[2],
+                                a[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, qf[kk][nt][0],
+                                                                   qf[kk][nt][1]);
+                }
+                // ---- mask, scale (log2 units), online softmax per column
+                uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float pr[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = key0 + lane / 4 + 8 * (e >> 1);
+                        sc[nt][e] = key < lim[nt][e & 1] ? sc[nt][e] * p.scale_log2 : -INFINITY;
+                    }
+#pragma unroll
+                    for (int ce = 0; ce < 2; ++ce) {
+                        float mx = fmaxf(sc[nt][ce], sc[nt][ce + 2]);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float m_new = fmaxf(m_run[nt][ce], mx);
+                        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                        const float corr = ex2(m_run[nt][ce] - m_use);
+                        pr[ce] = ex2(sc[nt][ce] - m_use);
+                        pr[ce + 2] = ex2(sc[nt][ce + 2] - m_use);
+                        l_run[nt][ce] = l_run[nt][ce] * corr + pr[ce] + pr[ce + 2];
+                        m_run[nt][ce] = m_new;
+#pragma unroll
+                        for (int dt = 0; dt < KSTEPS; ++dt) {
+                            acc[dt][nt][ce] *= corr;
+                            acc[dt][nt][ce + 2] *= corr;
+                        }
+                    }
+                    // P (rows = keys lane/4 and +8, cols 2*(lane%4)+{0,1}) as bf16 hi + lo,
+                    // transposed into the B-fragment layout of the PV product.
+                    const __nv_bfloat162 h01 = __floats2bfloat162_rn(pr[0], pr[1]);
+                    const __nv_bfloat162 h23 = __floats2bfloat162_rn(pr[2], pr[3]);
+                    const float2 f01 = __bfloat1622float2(h01);
+                    const float2 f23 = __bfloat1622float2(h23);
+                    bh[nt][0] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&h01));
+                    bh[nt][1] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&h23));
+                    bl[nt][0] = movmatrix_trans(pack_bf16(pr[0] - f01.x, pr[1] - f01.y));
+                    bl[nt][1] = movmatrix_trans(pack_bf16(pr[2] - f23.x, pr[3] - f23.y));
+                }
+                // ---- O^T += V^T . P^T
+                // Key index of the low half of a0/a1 (and +8 for a2/a3).
+                const int kq = 2 * (lane % 4);
+                uint32_t keep01 = 0xffffffffu, keep23 = 0xffffffffu;
+                if (valid < 16) {
+                    keep01 = (kq < valid ? 0x0000ffffu : 0u) | (kq + 1 < valid ? 0xffff0000u : 0u);
+                    keep23 = (kq + 8 < valid ? 0x0000ffffu : 0u) |
+                             (kq + 9 < valid ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int dt = 0; dt < KSTEPS; ++dt) {
+                    const int key = 16 * warp + (lane & 7) + (lane >> 4) * 8;
+                    const int d = dt * 16 + ((lane >> 3) & 1) * 8;
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(vt + (d / 64) * SLAB + sw128(key, (d % 64) / 8), a[0], a[1],
+                                      a[2], a[3]);
+                    // Keys past the split end may hold stale or NaN rows: zero them.
+                    a[0] &= keep01;
+                    a[1] &= keep01;
+                    a[2] &= keep23;
+                    a[3] &= keep23;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_bf16_16816(acc[dt][nt], a, bh[nt][0], bh[nt][1]);
+                        mma_bf16_16816(acc[dt][nt], a, bl[nt][0], bl[nt][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+        // Full column sums: lanes sharing lane%4 hold the same columns.
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int ce = 0; ce < 2; ++ce) {
+                float l = l_run[nt][ce];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                l_run[nt][ce] = l;
+            }
+    }
+
+    const bool any_failed = __syncthreads_or(failed) != 0;
+    if (any_failed && threadIdx.x == 0) record(p.status, ATLAS_DEV_TIMEOUT);
+
+    // Reuse the ring as combine scratch (all loads have landed or been drained).
+    float *cm = reinterpret_cast<float *>(smem);
+    float *cl = cm + kConsumerWarps * NCOLS;
+    float *cacc = cl + kConsumerWarps * NCOLS;
+    if (!any_failed && warp < kConsumerWarps) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int ce = 0; ce < 2; ++ce) {
+                const int c = nt * 8 + 2 * (lane % 4) + ce;
+                if (lane < 4) {
+                    cm[warp * NCOLS + c] = m_run[nt][ce];
+                    cl[warp * NCOLS + c] = l_run[nt][ce];
+                }
+#pragma unroll
+                for (int dt = 0; dt < KSTEPS; ++dt) {
+                    const int d = dt * 16 + lane / 4;
+                    cacc[(warp * NCOLS + c) * D + d] = acc[dt][nt][ce];
+                    cacc[(warp * NCOLS + c) * D + d + 8] = acc[dt][nt][ce + 2];
+                }
+            }
+    }
+    __syncthreads();
+    write_partials<kConsumerWarps, NCOLS, D>(p, cm, cl, cacc, col0, ncols, any_failed);
+}
+
+// ---------------------------------------------------------------- f32 path
+// Plain FFMA: each warp takes every 4th key of the split, lanes split the head
+// dimension, scores are warp all-reduces; up to 8 columns per CTA.
+template <int D>
+__global__ void __launch_bounds__(128)
+    split_f32_kernel(const SplitParams p) {
+    constexpr int NC = 8;
+    constexpr int W = 4;
+    constexpr int DPL = D / 32;
+    __shared__ float cm[W * NC], cl[W * NC];
+    __shared__ float cacc[W * NC * D];
+
+    int L, kv_begin, kv_end, col0, ncols;
+    if (!split_prologue<NC>(p, L, kv_begin, kv_end, col0, ncols)) return;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int b = blockIdx.z;
+    const int hkv = blockIdx.y / p.col_tiles;
+    const float *kp = static_cast<const float *>(p.k_pages);
+    const float *vp = static_cast<const float *>(p.v_pages);
+
+    float qv[NC][DPL], accv[NC][DPL], m_run[NC], l_run[NC];
+    int lim[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const bool ok = c < ncols;
+        const float *qrow = ok ? static_cast<const float *>(p.q) +
+                                     column_row(p, b, hkv, col0 + c) * D
+                               : nullptr;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) {
+            qv[c][j] = ok ? qrow[lane * DPL + j] : 0.f;
+            accv[c][j] = 0.f;
+        }
+        lim[c] = ok ? min(kv_end, column_visible(p, L, col0 + c)) : 0;
+        m_run[c] = -INFINITY;
+        l_run[c] = 0.f;
+    }
+    for (int t = kv_begin + warp; t < kv_end; t += W) {
+        const int phys = p.page_table[(int64_t)b * p.max_pages + t / p.P];
+        const int64_t base = (((int64_t)phys * p.Hkv + hkv) * p.P + t % p.P) * D + lane * DPL;
+        float kr[DPL], vr[DPL];
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) {
+            kr[j] = kp[base + j];
+            vr[j] = vp[base + j];
+        }
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            if (t >= lim[c]) continue;  // warp-uniform
+            float dot = 0.f;
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) dot = fmaf(qv[c][j], kr[j], dot);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            const float s2 = dot * p.scale_log2;
+            const float m_new = fmaxf(m_run[c], s2);
+            const float corr = ex2(m_run[c] - m_new);
+            const float pw = ex2(s2 - m_new);
+            l_run[c] = l_run[c] * corr + pw;
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) accv[c][j] = fmaf(pw, vr[j], accv[c][j] * corr);
+            m_run[c] = m_new;
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        if (lane == 0) {
+            cm[warp * NC + c] = m_run[c];
+            cl[warp * NC + c] = l_run[c];
+        }
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) cacc[(warp * NC + c) * D + lane * DPL + j] = accv[c][j];
+    }
+    __syncthreads();
+    write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, false);
+}
+
+template <int D, int NT, int STAGES>
+cudaError_t launch_bf16_instance(const SplitParams &p, const CUtensorMap &tmK,
+                                 const CUtensorMap &tmV, cudaStream_t stream) {
+    using Lay = SplitLayout<D, NT, STAGES>;
+    auto kern = split_bf16_kernel<D, NT, STAGES>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && !configured[dev]) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+        if (err != cudaSuccess) return err;
+        configured[dev] = 1;
+    }
+    dim3 grid(p.n_chunks, p.Hkv * p.col_tiles, p.B);
+    kern<<<grid, kSplitThreads, Lay::kBytes, stream>>>(tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int split_bf16_cols_per_cta(int G, int q_len) { return G * q_len <= 8 ? 8 : 16; }
+
+cudaError_t launch_split_bf16(const SplitParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                              cudaStream_t stream) {
+    const bool wide = split_bf16_cols_per_cta(p.G, p.q_len) == 16;
+    if (p.D == 128) {
+        return wide ? launch_bf16_instance<128, 2, 3>(p, tmK, tmV, stream)
+                    : launch_bf16_instance<128, 1, 3>(p, tmK, tmV, stream);
+    }
+    return wide ? launch_bf16_instance<64, 2, 4>(p, tmK, tmV, stream)
+                : launch_bf16_instance<64, 1, 4>(p, tmK, tmV, stream);
+}
+
+cudaError_t launch_split_f32(const SplitParams &p, cudaStream_t stream) {
+    dim3 grid(p.n_chunks, p.Hkv * p.col_tiles, p.B);
+    if (p.D == 128) split_f32_kernel<128><<<grid, 128, 0, stream>>>(p);
+    else split_f32_kernel<64><<<grid, 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace atlas

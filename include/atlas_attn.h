@@ -1,0 +1,158 @@
+/*
+ * atlas_attn.h -- exact causal grouped-query softmax attention over paged K/V,
+ * on one GB300 (sm_103a).
+ *
+ * What every entry point computes.  For each sequence b, query head h and query
+ * row i in [0, q_len):
+ *
+ *   kv head      g = h / (n_q_heads / n_kv_heads)       (contiguous GQA groups)
+ *   position     pos = seq_lens[b] - q_len + i          (the queries are the last
+ *                                                        q_len positions of K/V)
+ *   key t        k_t = k_pages[page_table[b][t / page_tokens]][g][t % page_tokens][:]
+ *   out[b][h][i] = sum_{t <= pos} exp(s_t - M) v_t / sum_{t <= pos} exp(s_t - M),
+ *                  s_t = scale * <q[b][h][i], k_t>,  M = max_t s_t
+ *   lse[b][h][i] = M + ln sum_{t <= pos} exp(s_t - M)     (natural log)
+ *
+ * Sources (page title, section):
+ *   CFR-Atlas README, "Core contract": folding exact pages into an online-softmax
+ *     state gives the full-KV result, which is what is computed here;
+ *   CFR-Atlas README, "Minimal integration": row-major K[token][dim], V[token][dim]
+ *     pages per (layer, K/V head, token range) -> the page pools below;
+ *   CPUAttn README, "Parallel example" and "Operator model": queries are the
+ *     suffix of K/V (positions start at SKV - SQ); decode is the same pattern
+ *     with one query row; split-K is combined by a structured merge;
+ *   ferrox-core crate index: causal_gqa_attention_paged (decode) and
+ *     causal_gqa_attention_prefill (prefill) name the two ends of this family.
+ *
+ * Layouts (all dense, row-major, C order; every pointer 16-byte aligned):
+ *   q, out        [batch][n_q_heads][q_len][head_dim]
+ *   k_pages,
+ *   v_pages       [num_pages][n_kv_heads][page_tokens][head_dim]
+ *   page_table    int32 [batch][max_pages_per_seq]; entries past a sequence's
+ *                 last page are never read
+ *   seq_lens      int32 [batch]; keys visible to the last query row
+ *   lse           float [batch][n_q_heads][q_len]
+ *
+ * Ownership and asynchrony.  Every tensor pointer is a DEVICE pointer owned by
+ * the caller; q, pools, page_table and seq_lens are only read.  The library
+ * allocates no device memory and keeps no per-call state (it caches a driver
+ * entry point and per-device kernel attributes).  All work is enqueued on
+ * `stream`; no call synchronises with the host.
+ *
+ * Supported: head_dim 64 or 128; page_tokens a power of two in [8, 128];
+ *   n_q_heads a multiple of n_kv_heads;
+ *   q/K/V float32 -> out float32, or q/K/V bfloat16 -> out bfloat16 or float32.
+ *   Accumulation and softmax state are float32 in every mode.
+ *
+ * Errors.  Host-side checks return a status before anything is enqueued.
+ * Data-dependent problems are found on the device: a page id outside
+ * [0, num_pages), a seq_len below q_len or above max_pages_per_seq*page_tokens,
+ * or a bounded wait that ran out each OR a bit (ATLAS_DEV_*) into *status_word
+ * (when given) and leave the affected output rows NaN.  The caller reads the
+ * word after synchronising the stream.  Non-finite inputs are not scanned for;
+ * they propagate into the rows that see them.
+ */
+#ifndef ATLAS_ATTN_H
+#define ATLAS_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATLAS_OK = 0,
+    ATLAS_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misalignment, GQA ratio */
+    ATLAS_ERR_UNSUPPORTED = 2, /* head_dim / page_tokens / dtype not supported */
+    ATLAS_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    ATLAS_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+    ATLAS_ERR_DEVICE = 5       /* reserved for callers: a status word bit was set */
+} atlas_status;
+
+typedef enum { ATLAS_F32 = 0, ATLAS_BF16 = 1 } atlas_dtype;
+
+typedef enum { ATLAS_KIND_DECODE = 0, ATLAS_KIND_SUFFIX = 1, ATLAS_KIND_PREFILL = 2 } atlas_kind;
+
+/* Bits the kernels OR into *status_word. */
+#define ATLAS_DEV_BAD_PAGE 1u    /* a page id outside [0, num_pages) */
+#define ATLAS_DEV_BAD_SEQLEN 2u  /* seq_len < q_len or > max_pages_per_seq * page_tokens */
+#define ATLAS_DEV_TIMEOUT 4u     /* a bounded wait inside a kernel ran out */
+
+/* Test-only: make the decode producer withhold one stage so that the consumers'
+ * bounded wait runs out and ATLAS_DEV_TIMEOUT is reported. */
+#define ATLAS_DEBUG_WITHHOLD_STAGE 1u
+
+/* Everything a call needs beyond the (q, k_pages, v_pages, page_table,
+ * seq_lens, n_q_heads, n_kv_heads, head_dim, page_tokens, scale) list. */
+typedef struct {
+    int32_t batch;             /* B >= 1 */
+    int32_t max_pages_per_seq; /* page_table row length */
+    int32_t num_pages;         /* pages in each pool */
+    int32_t q_len;             /* 1 for decode, SQ for suffix, S for prefill */
+    atlas_dtype q_dtype;       /* must equal kv_dtype */
+    atlas_dtype kv_dtype;
+    atlas_dtype out_dtype;
+    void *out;                 /* [B][Hq][q_len][D] of out_dtype; written */
+    float *lse;                /* optional [B][Hq][q_len]; NULL to skip */
+    void *workspace;           /* device scratch, >= atlas_attn_workspace_size() bytes */
+    size_t workspace_bytes;
+    uint32_t *status_word;     /* optional device word; bits OR-ed, never cleared */
+    void *stream;              /* cudaStream_t; NULL = the legacy default stream */
+    int32_t split_tokens;      /* keys per split-KV chunk; 0 = automatic; else a
+                                  multiple of 64 */
+    uint32_t debug_flags;      /* 0 in production; ATLAS_DEBUG_* for tests */
+    void *const *events;       /* optional host array of 3 cudaEvent_t, recorded on
+                                  `stream` before the main kernel, between it and the
+                                  merge, and after the merge (profiling); NULL = none */
+} atlas_launch;
+
+/*
+ * atlas_attn_decode: one query row per sequence (L->q_len must be 1), the
+ * decode step over a paged cache (ferrox-core "causal_gqa_attention_paged";
+ * CPUAttn "Operator model": decode is kv_cache=True with one query row).
+ * Split-KV over the page stream, then a log-sum-exp merge.
+ */
+atlas_status atlas_attn_decode(const void *q, const void *k_pages, const void *v_pages,
+                               const int32_t *page_table, const int32_t *seq_lens,
+                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                               int32_t page_tokens, float scale, const atlas_launch *L);
+
+/*
+ * atlas_attn_suffix: L->q_len query rows per sequence that are the last q_len
+ * positions of its K/V (CPUAttn README, "Parallel example": kv_cache=True,
+ * positions start at SKV - SQ).  Row i sees keys 0 .. seq_len - q_len + i.
+ */
+atlas_status atlas_attn_suffix(const void *q, const void *k_pages, const void *v_pages,
+                               const int32_t *page_table, const int32_t *seq_lens,
+                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                               int32_t page_tokens, float scale, const atlas_launch *L);
+
+/*
+ * atlas_attn_prefill: causal self-attention of a whole prompt whose K/V were
+ * written into pages (ferrox-core "causal_gqa_attention_prefill").  Every
+ * seq_lens[b] must equal L->q_len; a sequence where it does not gets
+ * ATLAS_DEV_BAD_SEQLEN and NaN rows.
+ */
+atlas_status atlas_attn_prefill(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *page_table, const int32_t *seq_lens,
+                                int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                int32_t page_tokens, float scale, const atlas_launch *L);
+
+/*
+ * Bytes of device workspace the call of `kind` with these arguments needs (0 if
+ * none).  Reads batch, max_pages_per_seq, q_len, the dtypes and split_tokens
+ * from *L; ignores its pointers.  Returns SIZE_MAX if the arguments are invalid.
+ */
+size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,
+                                 int32_t head_dim, int32_t page_tokens, const atlas_launch *L);
+
+/* Static, human-readable text for a status code. */
+const char *atlas_attn_status_string(atlas_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATLAS_ATTN_H */

@@ -1,0 +1,117 @@
+"""CPU-side checks of the C ABI: the library builds and loads, exports every
+function include/atlas_attn.h declares, and its host-only logic (argument
+checks, workspace sizing, status strings) behaves as documented.  No kernel is
+launched: every call here returns before any CUDA work."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_causal_gqa_gb300 as atlas
+from exact_causal_gqa_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return atlas.load_library()
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(atlas_attn_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("atlas_attn_decode", "atlas_attn_suffix", "atlas_attn_prefill",
+              "atlas_attn_workspace_size", "atlas_attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\w+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, f"not exported: {missing}"
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert atlas.status_string(code)
+    assert atlas.status_string(99) == "unknown status"
+
+
+def launch(**kw):
+    L = atlas._Launch()
+    L.batch, L.max_pages_per_seq, L.num_pages, L.q_len = 2, 8, 16, 1
+    L.q_dtype = L.kv_dtype = L.out_dtype = 1
+    for k, v in kw.items():
+        setattr(L, k, v)
+    return L
+
+
+def ws(lib, kind=0, Hq=8, Hkv=2, D=128, P=16, **kw):
+    L = launch(**kw)
+    return lib.atlas_attn_workspace_size(kind, Hq, Hkv, D, P, ctypes.byref(L))
+
+
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+
+def test_workspace_size_matches_the_split_layout(lib):
+    # 2 sequences x 8 q heads x 1 row, context <= 128 keys, 64-key splits -> 2 splits
+    n = ws(lib, split_tokens=64)
+    rows, splits, D = 2 * 8, 2, 128
+    acc = rows * splits * D * 4
+    assert n == (acc + 255) // 256 * 256 + rows * splits * 2 * 4
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Hq=6, Hkv=4), SIZE_MAX),          # Hq not a multiple of Hkv
+    (dict(D=96), SIZE_MAX),                 # unsupported head_dim
+    (dict(P=12), SIZE_MAX),                 # page_tokens not a power of two
+    (dict(P=256), SIZE_MAX),                # page_tokens above 128
+    (dict(q_len=2), SIZE_MAX),              # decode takes one query row
+    (dict(split_tokens=100), SIZE_MAX),     # splits must be multiples of 64
+    (dict(out_dtype=0, q_dtype=0, kv_dtype=1), SIZE_MAX),  # q and K/V dtypes differ
+    (dict(kv_dtype=0, q_dtype=0, out_dtype=1), SIZE_MAX),  # f32 K/V only gives f32 out
+])
+def test_invalid_plans_are_rejected(lib, kw, expect):
+    assert ws(lib, **kw) == expect
+
+
+def test_entry_points_check_arguments_before_any_launch(lib):
+    L = launch()
+    args = [None] * 5 + [8, 2, 128, 16, ctypes.c_float(0.1), ctypes.byref(L)]
+    for name in ("atlas_attn_decode", "atlas_attn_suffix", "atlas_attn_prefill"):
+        assert getattr(lib, name)(*args) == 1  # null pointers -> ATLAS_ERR_INVALID_ARG
+    # misaligned pointers are rejected too
+    fake = 0x1000
+    L.out = fake + 8
+    args = [fake, fake, fake, fake, fake, 8, 2, 128, 16, ctypes.c_float(0.1), ctypes.byref(L)]
+    assert lib.atlas_attn_decode(*args) == 1
+    # unsupported head_dim
+    L.out = fake
+    args = [fake, fake, fake, fake, fake, 8, 2, 80, 16, ctypes.c_float(0.1), ctypes.byref(L)]
+    assert lib.atlas_attn_decode(*args) == 2
+    # missing workspace
+    args = [fake, fake, fake, fake, fake, 8, 2, 128, 16, ctypes.c_float(0.1), ctypes.byref(L)]
+    assert lib.atlas_attn_decode(*args) == 3
+    # non-finite scale
+    args = [fake, fake, fake, fake, fake, 8, 2, 128, 16, ctypes.c_float(float("nan")),
+            ctypes.byref(L)]
+    assert lib.atlas_attn_decode(*args) == 1

@@ -1,0 +1,162 @@
+"""Parity of the split-KV decode path (and its LSE merge) with the fp64 oracle,
+through the C ABI, on the same seeded host bytes.  Needs a GB300."""
+import numpy as np
+import pytest
+import torch
+
+import exact_causal_gqa_gb300 as atlas
+from exact_causal_gqa_gb300 import inputs
+from tests.gpu_helpers import assert_parity, flat_rows, oracle_rows, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def small(kind="decode", B=3, Hq=8, Hkv=2, D=128, P=16, lens=(100, 257, 16), q_len=None,
+          dtype="bf16", seed=0, **kw):
+    return inputs.make(kind, B, Hq, Hkv, D, P, list(lens), q_len=q_len, dtype=dtype, seed=seed,
+                       **kw)
+
+
+CASES = [
+    # (D, P, Hq, Hkv, lens) -- page boundaries and +-1, several splits and tails
+    (128, 16, 8, 2, (1, 15, 16, 17, 64, 65, 1000)),
+    (128, 8, 4, 4, (7, 8, 9, 300)),
+    (128, 32, 32, 4, (31, 32, 33, 511)),
+    (128, 64, 16, 2, (63, 64, 65, 4097)),
+    (128, 128, 8, 8, (127, 128, 129, 2000)),
+    (64, 16, 4, 1, (5, 16, 700)),
+    (64, 64, 16, 1, (64, 65, 1234)),
+    (128, 16, 16, 1, (333, 48)),          # G = 16: two column tiles of 8 in one CTA
+]
+
+
+@pytest.mark.parametrize("D,P,Hq,Hkv,lens", CASES)
+@pytest.mark.parametrize("split", [0, 64, 192])
+def test_decode_bf16_parity(D, P, Hq, Hkv, lens, split):
+    prob = small(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, P=P, lens=lens, seed=D + P + Hq)
+    ref, ref_lse = oracle_rows(prob, want_lse=True)
+    dev = prob.to(DEV)
+    lse = torch.empty(flat_rows(prob), dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out32 = run_gpu(dev, out_dtype=torch.float32, lse=lse, status=status, split_tokens=split)
+    out16 = run_gpu(dev, out_dtype=torch.bfloat16, split_tokens=split)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_parity(prob, out32, ref, "f32 out")
+    assert_parity(prob, out16, ref, "bf16 out")
+    # the bf16 store is the RNE of the f32 result of the same split plan
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.reshape(-1), rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("split", [0, 64])
+def test_decode_f32_parity(D, split):
+    prob = small(B=4, Hq=8, Hkv=4, D=D, P=16, lens=(1, 17, 512, 777), dtype="f32", seed=D)
+    ref, ref_lse = oracle_rows(prob, want_lse=True)
+    lse = torch.empty(flat_rows(prob), dtype=torch.float32, device=DEV)
+    out = run_gpu(prob.to(DEV), lse=lse, split_tokens=split)
+    assert_parity(prob, out, ref, "f32")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.reshape(-1), rtol=0, atol=1e-5)
+
+
+def test_config1_full_parity():
+    prob = inputs.make_config(1)
+    ref = oracle_rows(prob)
+    out = run_gpu(prob.to(DEV))
+    assert_parity(prob, out, ref, "config 1")
+
+
+@pytest.mark.parametrize("index", [2, 3])
+def test_full_size_decode_sampled_rows(index):
+    prob = inputs.make_config(index)
+    dev = prob.to(DEV)
+    out = run_gpu(dev)
+    out32 = run_gpu(dev, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(index)
+    rows = np.unique(np.concatenate([rng.choice(flat_rows(prob), 48, replace=False),
+                                     [0, flat_rows(prob) - 1]]))
+    ref = oracle_rows(prob, rows=rows)
+    D = prob.head_dim
+    assert_parity(prob, out.reshape(-1, D)[torch.from_numpy(rows).to(DEV)], ref, "bf16 out")
+    assert_parity(prob, out32.reshape(-1, D)[torch.from_numpy(rows).to(DEV)], ref, "f32 out")
+    assert torch.equal(out, out32.to(torch.bfloat16))
+    assert torch.isfinite(out32).all()
+
+
+def test_page_permutation_is_bitwise_invariant():
+    prob = small(lens=(300, 45, 129), P=16, extra_pages=5)
+    dev = prob.to(DEV)
+    base = run_gpu(dev, out_dtype=torch.float32)
+    # move every page to a new slot and rewrite the table accordingly
+    perm = torch.randperm(prob.num_pages, generator=torch.Generator().manual_seed(5))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(prob.num_pages)
+    k2 = torch.empty_like(prob.k_pages)
+    v2 = torch.empty_like(prob.v_pages)
+    k2[inv] = prob.k_pages
+    v2[inv] = prob.v_pages
+    table2 = inv[prob.page_table.long()].to(torch.int32)
+    prob2 = inputs.Problem(**{**prob.__dict__, "k_pages": k2, "v_pages": v2,
+                              "page_table": table2})
+    again = run_gpu(prob2.to(DEV), out_dtype=torch.float32)
+    assert torch.equal(base, again)
+
+
+def test_deterministic_and_padding_never_read():
+    prob = small(lens=(1000, 3, 640), pad_page=10 ** 6)  # padding ids are out of range
+    dev = prob.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    a = run_gpu(dev, status=status)
+    b = run_gpu(dev, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(a, b)
+
+
+def test_bad_page_id_flags_status_and_poisons_only_that_sequence():
+    prob = small(lens=(100, 200, 50))
+    prob.page_table[1, 3] = prob.num_pages + 7
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & atlas.DEV_BAD_PAGE
+    assert torch.isnan(out[1]).all()
+    assert torch.isfinite(out[0]).all() and torch.isfinite(out[2]).all()
+
+
+def test_bad_seq_len_flags_status_and_poisons_rows():
+    prob = small(lens=(100, 200, 50))
+    prob.seq_lens[2] = prob.max_pages * prob.page_tokens + 1
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & atlas.DEV_BAD_SEQLEN
+    assert torch.isnan(out[2]).all()
+    assert torch.isfinite(out[:2]).all()
+
+
+def test_small_workspace_is_rejected():
+    prob = small().to(DEV)
+    with pytest.raises(atlas.AtlasError) as e:
+        run_gpu(prob, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    assert e.value.status == 3
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    # The producer withholds its first stage: the consumers' bounded wait runs
+    # out (about 2 s), the kernel records ATLAS_DEV_TIMEOUT and returns.
+    prob = small(B=1, lens=(300,))
+    dev = prob.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(dev, out_dtype=torch.float32, status=status,
+                  debug_flags=atlas.DEBUG_WITHHOLD_STAGE)
+    torch.cuda.synchronize()
+    assert int(status.item()) & atlas.DEV_TIMEOUT
+    assert torch.isnan(out).all()
+    ref = oracle_rows(prob)
+    good = run_gpu(dev, out_dtype=torch.float32)
+    assert_parity(prob, good, ref, "after timeout")
