@@ -41,12 +41,15 @@ L2_BYTES = 129 * 1024 * 1024
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["atlas", "reference"], default="atlas")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--split-tokens", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller profiling captures)")
     return ap.parse_args()
 
 
@@ -95,7 +98,7 @@ def traffic_record(kernel: str, workload: str):
 
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -124,25 +127,33 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
+    def summary(self, t_begin: float, t_end: float):
+        """Median SM clock and the throttle reasons seen in samples stamped inside
+        [t_begin, t_end] (host wall-clock seconds)."""
+        import datetime
         if not self.lines:
             return None
-        sm, mx, reasons = [], [], set()
+        sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             f = [x.strip() for x in line.split(",")]
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if not (t_begin <= ts <= t_end):
+                    continue
+                sm.append(float(f[2]))
+                mx.append(float(f[3]))
+                power.append(float(f[4]))
             except (ValueError, IndexError):
                 continue
-            for name, val in zip(names, f[5:9]):
+            for name, val in zip(names, f[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "power_w": statistics.median(power), "reasons": sorted(reasons),
+                "samples": len(sm)}
 
 
 def run_atlas(args, world, rank, local):
@@ -154,7 +165,8 @@ def run_atlas(args, world, rank, local):
     atlas.load_library()
     cfg = inputs.CONFIGS[args.config]
     seed = args.config + 1000 * rank
-    prob = inputs.make_config(args.config, seed=seed, device=dev)
+    overrides = {"B": args.batch} if args.batch else {}
+    prob = inputs.make_config(args.config, seed=seed, device=dev, **overrides)
     kv_bytes, flops = work_of(prob)
     out_dtype = torch.bfloat16 if prob.out_dtype == "bf16" else torch.float32
     out = torch.empty(prob.q.shape, dtype=out_dtype, device=dev)
@@ -180,10 +192,18 @@ def run_atlas(args, world, rank, local):
 
     step_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     step_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
+        # Untimed steps for about a second so the clock sampler sees the GPU under
+        # this load even when the timed region is shorter than its period.
+        settle_end = time.time() + 1.0
+        while time.time() < settle_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        t_begin = time.time()
         t0 = time.perf_counter()
         for k in range(args.steps):
             if flush is not None:
@@ -193,6 +213,8 @@ def run_atlas(args, world, rank, local):
             step_end[k].record()
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
+        t_end = time.time()
+        time.sleep(0.3)
     if world > 1:
         torch.distributed.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(step_start, step_end)]
@@ -270,7 +292,7 @@ def run_atlas(args, world, rank, local):
         "dtype": prob.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
         "config": {
-            "workload": cfg["name"],
+            "workload": cfg["name"] if not args.batch else f'{cfg["name"]} (batch {args.batch})',
             "kind": prob.kind, "batch": prob.batch, "n_q_heads": prob.n_q_heads,
             "n_kv_heads": prob.n_kv_heads, "head_dim": prob.head_dim,
             "page_tokens": prob.page_tokens, "q_len": prob.q_len,
@@ -298,7 +320,12 @@ def run_atlas(args, world, rank, local):
         "gpu_launches": 2 * args.steps,
         "device_status": status_val,
     }
-    clk = clocks.summary()
+    # Samples of the timed region; if it was shorter than the 200 ms period, the
+    # last half second of the identical untimed loop just before it.
+    clk = clocks.summary(t_begin, t_end + 0.05) or clocks.summary(t_begin - 0.5, t_end + 0.05)
+    if clk is not None:
+        clk["window"] = "timed region" if clocks.summary(t_begin, t_end + 0.05) else \
+            "last 0.5 s of the identical untimed loop + timed region"
     line["clocks"] = clk
     if e2e is not None:
         e_ms, bi, bo = e2e
@@ -306,7 +333,8 @@ def run_atlas(args, world, rank, local):
             (world * flops / (e_ms * 1e-3) / 1e12)
         line["e2e"] = {"value": round(e_val, 3), "unit": unit, "ms_per_step": round(e_ms, 4),
                        "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
-    line["cpu_baseline"] = cpu_baseline(args.config, prob, decode_like)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config, prob, decode_like)
     return line
 
 

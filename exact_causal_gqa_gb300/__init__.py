@@ -209,6 +209,8 @@ class EventTimer:
 
     def __init__(self):
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in self.ev:  # torch creates the CUDA event on its first record
+            e.record()
         self.handles = (ctypes.c_void_p * 3)(*[e.cuda_event for e in self.ev])
 
     def main_ms(self) -> float:

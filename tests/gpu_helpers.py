@@ -4,9 +4,10 @@ the same host bytes, and apply the tolerance rule.
 Tolerances (written here once, used by every parity test):
   * f32 q/K/V:  max|gpu - ref| <= 1e-5 * max|ref| over the output tensor;
   * bf16 q/K/V, f32 output:  max|gpu - ref| <= 2e-3 (absolute);
-  * bf16 output:  |gpu - ref| <= 2e-3 + 2^-9 |ref| elementwise -- the bf16 store
-    alone rounds by up to 2^-9 |o| -- and the bf16 result must equal the
-    round-to-nearest-even of the f32-output result of the same call bit for bit.
+  * bf16 output:  |gpu - ref| <= 2e-3 + 2^-8 |ref| elementwise -- bf16 keeps 8
+    significant bits, so the store alone rounds by up to 2^-8 |o| (its unit
+    roundoff) -- and the bf16 result must equal the round-to-nearest-even of the
+    f32-output result of the same call bit for bit.
 """
 import numpy as np
 import torch
@@ -16,7 +17,7 @@ import oracle
 
 F32_REL = 1e-5
 BF16_ABS = 2e-3
-BF16_STORE_REL = 2.0 ** -9
+BF16_STORE_REL = 2.0 ** -8
 
 
 def oracle_rows(prob, rows=None, want_lse=False):
@@ -43,7 +44,7 @@ def assert_parity(prob, got, ref, label=""):
     else:
         lim = BF16_ABS + BF16_STORE_REL * np.abs(ref)
         worst = (err - lim).max()
-        assert worst <= 0, f"{label}: err exceeds 2e-3 + 2^-9|ref| by {worst:.3e}"
+        assert worst <= 0, f"{label}: err exceeds 2e-3 + 2^-8|ref| by {worst:.3e}"
     return float(err.max())
 
 
