@@ -151,6 +151,39 @@ size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_k
 /* Static, human-readable text for a status code. */
 const char *atlas_attn_status_string(atlas_status status);
 
+/* Size of the library-owned device scratch used by atlas_attn_decode_static_scratch. */
+#define ATLAS_STATIC_SCRATCH_BYTES (16u << 20) /* 16 MiB per GPU that loads the library */
+
+/*
+ * atlas_attn_decode_static_scratch: atlas_attn_decode for callers that cannot
+ * allocate device memory on the decode path (a host framework that owns all
+ * device memory and forbids other allocations, or a serving loop where
+ * cudaMalloc/cudaFree may synchronise the device).  The pages have no
+ * counterpart to this entry point; it exists for such integrations.
+ *
+ * Same arguments and results as atlas_attn_decode, except that L->workspace and
+ * L->workspace_bytes are ignored: the split-KV scratch lives in a fixed
+ * ATLAS_STATIC_SCRATCH_BYTES array of device memory owned by the library (held
+ * on every GPU that loads the library until the process exits).  The call
+ * allocates nothing.  The caller still passes q, the pools, the page table,
+ * seq_lens and the output (and optionally lse / status_word).
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Returns ATLAS_ERR_WORKSPACE when the call would need
+ * more than ATLAS_STATIC_SCRATCH_BYTES of scratch (atlas_attn_workspace_size
+ * with ATLAS_KIND_DECODE gives the need), ATLAS_ERR_CUDA if the address lookup
+ * fails.  All calls on a device share the array: calls whose kernels may overlap
+ * on the GPU (unordered streams) race on it.  Nothing in it needs clearing
+ * between calls.
+ */
+atlas_status atlas_attn_decode_static_scratch(const void *q, const void *k_pages,
+                                              const void *v_pages, const int32_t *page_table,
+                                              const int32_t *seq_lens, int32_t n_q_heads,
+                                              int32_t n_kv_heads, int32_t head_dim,
+                                              int32_t page_tokens, float scale,
+                                              const atlas_launch *L);
+
 #ifdef __cplusplus
 }
 #endif
