@@ -32,6 +32,7 @@ KIND_DECODE, KIND_SUFFIX, KIND_PREFILL = 0, 1, 2
 _KINDS = {"decode": KIND_DECODE, "suffix": KIND_SUFFIX, "prefill": KIND_PREFILL}
 DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2, 4
 DEBUG_WITHHOLD_STAGE = 1
+DEBUG_TC_DIRECT = 2
 _F32, _BF16 = 0, 1
 _DTYPES = {torch.float32: _F32, torch.bfloat16: _BF16}
 STATUS_NAMES = {0: "ATLAS_OK", 1: "ATLAS_ERR_INVALID_ARG", 2: "ATLAS_ERR_UNSUPPORTED",

@@ -39,11 +39,19 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // sizes, so a given problem always gets the same split (and the same bits).
 constexpr int64_t kPlanCtas = 152 * 2 * 8;
 
-enum class Path { SplitBF16, SplitF32 };
+// The tensor-core path's split plan aims for 152 SMs x 1 CTA x 8 waves; it writes
+// the output directly once a call has at least this many query tiles.
+constexpr int64_t kTcPlanCtas = 152 * 8;
+constexpr int64_t kTcDirectTiles = 152 * 2;
+// Query tiles whose rows see fewer keys than this use a hi + lo split of P.
+constexpr int kHiLoBelow = 512;
+
+enum class Path { SplitBF16, SplitF32, TensorCore };
 
 struct Plan {
     Path path;
     int chunk, n_chunks, col_tiles, G;
+    int tc_split, tiles_per_unit, tiles_per_head;
     size_t acc_bytes, ml_offset, ws_bytes;
 };
 
@@ -77,6 +85,42 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
 
     const int G = Hq / Hkv;
     plan->G = G;
+    plan->tc_split = 0;
+    plan->tiles_per_unit = plan->tiles_per_head = 0;
+    if (L->kv_dtype == ATLAS_BF16 && D == 128 && (int64_t)G * L->q_len > 16) {
+        // Many query rows per (sequence, kv head): 128-row tiles on tcgen05.
+        plan->path = Path::TensorCore;
+        const int64_t tiles_per_unit = ((int64_t)G * L->q_len + 127) / 128;
+        const int64_t tiles = (int64_t)L->batch * Hkv * tiles_per_unit;
+        if ((int64_t)L->batch * Hq * L->q_len >= INT32_MAX) return ATLAS_ERR_INVALID_ARG;
+        plan->tiles_per_unit = (int)tiles_per_unit;
+        plan->col_tiles = 0;
+        int64_t chunk = 0;
+        if (L->split_tokens > 0) {
+            chunk = round_up(L->split_tokens, 128);
+        } else if (tiles < kTcDirectTiles && !(L->debug_flags & ATLAS_DEBUG_TC_DIRECT)) {
+            chunk = round_up((max_ctx * tiles + kTcPlanCtas - 1) / kTcPlanCtas, 128);
+            if (chunk < 1024) chunk = 1024;
+            if (chunk > 16384) chunk = 16384;
+        }
+        if (chunk > 0) {
+            if (chunk > round_up(max_ctx, 128)) chunk = round_up(max_ctx, 128);
+            if (tiles > 65535) return ATLAS_ERR_UNSUPPORTED;
+            plan->tc_split = 1;
+            plan->chunk = (int)chunk;
+            plan->n_chunks = (int)((max_ctx + chunk - 1) / chunk);
+            const int64_t rows = (int64_t)L->batch * Hq * L->q_len;
+            plan->acc_bytes = (size_t)rows * plan->n_chunks * D * sizeof(float);
+            plan->ml_offset = (size_t)round_up((int64_t)plan->acc_bytes, 256);
+            plan->ws_bytes = plan->ml_offset + (size_t)rows * plan->n_chunks * 2 * sizeof(float);
+        } else {
+            if (tiles > INT32_MAX) return ATLAS_ERR_UNSUPPORTED;
+            plan->chunk = plan->n_chunks = 0;
+            plan->tiles_per_head = (L->q_len % 128 == 0) ? L->q_len / 128 : 0;
+            plan->acc_bytes = plan->ml_offset = plan->ws_bytes = 0;
+        }
+        return ATLAS_OK;
+    }
     plan->path = L->kv_dtype == ATLAS_BF16 ? Path::SplitBF16 : Path::SplitF32;
     const int cols = plan->path == Path::SplitBF16 ? split_bf16_cols_per_cta(G, L->q_len) : 8;
     plan->col_tiles = (G * L->q_len + cols - 1) / cols;
@@ -98,6 +142,23 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     plan->ml_offset = (size_t)round_up((int64_t)plan->acc_bytes, 256);
     plan->ws_bytes = plan->ml_offset + (size_t)rows * plan->n_chunks * 2 * sizeof(float);
     return ATLAS_OK;
+}
+
+// 2-D view of a bf16 tensor with D elements per row: `rows` rows; boxes of 64
+// elements x box_rows rows with 128-byte swizzling.
+atlas_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int32_t D,
+                             int32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return ATLAS_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 
 // 2-D view of a page pool: rows = num_pages*Hkv*P, D bf16 per row; boxes of
@@ -166,6 +227,49 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     if (L->events)
         for (int i = 0; i < 3; ++i) ev[i] = static_cast<cudaEvent_t>(L->events[i]);
     cudaError_t err;
+    if (plan.path == Path::TensorCore) {
+        CUtensorMap tmQ, tmK, tmV;
+        const int box = P < 128 ? P : 128;
+        st = encode_rows_map(&tmQ, q, (int64_t)L->batch * Hq * L->q_len, D, 128);
+        if (st == ATLAS_OK)
+            st = encode_rows_map(&tmK, k_pages, (int64_t)L->num_pages * Hkv * P, D, box);
+        if (st == ATLAS_OK)
+            st = encode_rows_map(&tmV, v_pages, (int64_t)L->num_pages * Hkv * P, D, box);
+        if (st != ATLAS_OK) return st;
+        TcParams tp{};
+        tp.page_table = page_table;
+        tp.seq_lens = seq_lens;
+        tp.B = L->batch;
+        tp.Hq = Hq;
+        tp.Hkv = Hkv;
+        tp.G = plan.G;
+        tp.P = P;
+        tp.q_len = L->q_len;
+        tp.max_pages = L->max_pages_per_seq;
+        tp.num_pages = L->num_pages;
+        tp.tiles_per_unit = plan.tiles_per_unit;
+        tp.tiles_per_head = plan.tiles_per_head;
+        tp.split = plan.tc_split;
+        tp.chunk = plan.chunk;
+        tp.n_chunks = plan.n_chunks;
+        tp.require_full = kind == ATLAS_KIND_PREFILL;
+        tp.hilo_below = kHiLoBelow;
+        tp.scale_log2 = scale * kLog2e;
+        tp.out = L->out;
+        tp.out_bf16 = L->out_dtype == ATLAS_BF16;
+        tp.lse = L->lse;
+        tp.ws_acc = sp.ws_acc;
+        tp.ws_ml = sp.ws_ml;
+        tp.status = L->status_word;
+        if (ev[0] && cudaEventRecord(ev[0], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+        err = launch_fmha_tc(tp, tmQ, tmK, tmV, stream);
+        if (err != cudaSuccess) return ATLAS_ERR_CUDA;
+        if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+        if (!plan.tc_split) {
+            if (ev[2] && cudaEventRecord(ev[2], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+            return ATLAS_OK;
+        }
+    } else {
     if (ev[0] && cudaEventRecord(ev[0], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
     if (plan.path == Path::SplitBF16) {
         CUtensorMap tmK, tmV;
@@ -178,6 +282,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     }
     if (err != cudaSuccess) return ATLAS_ERR_CUDA;
     if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+    }
 
     MergeParams mp{};
     mp.seq_lens = seq_lens;

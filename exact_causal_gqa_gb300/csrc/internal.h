@@ -49,6 +49,31 @@ struct MergeParams {
     float *lse;
 };
 
+// Tensor-core (tcgen05 / TMEM) path for many query rows per (sequence, kv head):
+// 128-row query tiles x 128-key blocks, head_dim 128, bf16.  Either writes the
+// normalised output directly (one CTA per tile, all its keys) or, when there are
+// too few tiles to fill the GPU, split partials in the SplitParams layout.
+struct TcParams {
+    const int32_t *page_table;
+    const int32_t *seq_lens;
+    int32_t B, Hq, Hkv, G, P, q_len, max_pages, num_pages;
+    int32_t tiles_per_unit;   // ceil(G * q_len / 128)
+    int32_t tiles_per_head;   // q_len / 128 when q_len % 128 == 0 (heavy-first order), else 0
+    int32_t split;            // 1: write split partials; 0: write the output
+    int32_t chunk, n_chunks;  // split geometry (chunk a multiple of 128)
+    int32_t require_full;
+    int32_t hilo_below;       // tiles whose rows see fewer keys use a hi+lo split of P
+    float scale_log2;
+    void *out;
+    int32_t out_bf16;
+    float *lse;
+    float *ws_acc, *ws_ml;
+    uint32_t *status;
+};
+
+cudaError_t launch_fmha_tc(const TcParams &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                           const CUtensorMap &tmV, cudaStream_t stream);
+
 // Columns handled by one CTA of the bf16 split kernel.
 int split_bf16_cols_per_cta(int G, int q_len);
 

@@ -83,6 +83,9 @@ typedef enum { ATLAS_KIND_DECODE = 0, ATLAS_KIND_SUFFIX = 1, ATLAS_KIND_PREFILL 
 /* Test-only: make the decode producer withhold one stage so that the consumers'
  * bounded wait runs out and ATLAS_DEV_TIMEOUT is reported. */
 #define ATLAS_DEBUG_WITHHOLD_STAGE 1u
+/* Test-only: the tensor-core path writes the output directly (no split-KV), even
+ * when the call has few query tiles. */
+#define ATLAS_DEBUG_TC_DIRECT 2u
 
 /* Everything a call needs beyond the (q, k_pages, v_pages, page_table,
  * seq_lens, n_q_heads, n_kv_heads, head_dim, page_tokens, scale) list. */

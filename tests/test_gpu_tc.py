@@ -1,0 +1,147 @@
+"""Parity of the tensor-core (tcgen05 / TMEM) suffix and prefill path with the
+fp64 oracle, through the C ABI, on the same seeded host bytes.  Needs a GB300."""
+import numpy as np
+import pytest
+import torch
+
+import exact_causal_gqa_gb300 as atlas
+from exact_causal_gqa_gb300 import inputs
+from tests.gpu_helpers import assert_parity, flat_rows, oracle_rows, run_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def check(prob, split=0, flags=0):
+    ref, ref_lse = oracle_rows(prob, want_lse=True)
+    dev = prob.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lse = torch.empty(flat_rows(prob), dtype=torch.float32, device=DEV)
+    out32 = run_gpu(dev, out_dtype=torch.float32, lse=lse, status=status, split_tokens=split,
+                    debug_flags=flags)
+    out16 = run_gpu(dev, out_dtype=torch.bfloat16, split_tokens=split, debug_flags=flags)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_parity(prob, out32, ref, "f32 out")
+    assert_parity(prob, out16, ref, "bf16 out")
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.reshape(-1), rtol=0, atol=2e-4)
+    return out32
+
+
+SUFFIX = [
+    # (B, Hq, Hkv, P, SQ, lens)
+    (3, 32, 4, 32, 16, (16, 300, 1000)),       # G*SQ = 128: one tile per (seq, kv head)
+    (2, 8, 1, 16, 16, (129, 4097)),            # one tile, P = 16
+    (2, 16, 2, 64, 4, (64, 777)),              # G*SQ = 32: a partial tile
+    (1, 16, 1, 128, 32, (1024,)),              # G*SQ = 512: four tiles, P = 128
+    (2, 12, 4, 8, 8, (33, 2000)),              # G = 3, G*SQ = 24, P = 8
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,P,SQ,lens", SUFFIX)
+@pytest.mark.parametrize("split", [0, 128, 384])
+def test_suffix_parity(B, Hq, Hkv, P, SQ, lens, split):
+    prob = inputs.make("suffix", B, Hq, Hkv, 128, P, list(lens), q_len=SQ, seed=B + Hq + P + SQ)
+    check(prob, split=split)
+
+
+PREFILL = [
+    # (B, Hq, Hkv, P, S)
+    (1, 4, 1, 64, 128),
+    (2, 4, 2, 64, 129),
+    (1, 8, 2, 16, 300),
+    (1, 2, 2, 128, 1000),
+    (2, 8, 8, 32, 640),
+    (1, 32, 8, 64, 100),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,P,S", PREFILL)
+@pytest.mark.parametrize("mode", ["direct", "split256", "auto"])
+def test_prefill_parity(B, Hq, Hkv, P, S, mode):
+    prob = inputs.make("prefill", B, Hq, Hkv, 128, P, [S] * B, seed=S + Hq + P)
+    split = 256 if mode == "split256" else 0
+    flags = atlas.DEBUG_TC_DIRECT if mode == "direct" else 0
+    check(prob, split=split, flags=flags)
+
+
+def test_prefill_direct_is_deterministic_and_page_order_invariant():
+    prob = inputs.make("prefill", 2, 8, 2, 128, 32, [700, 700], seed=9, extra_pages=3)
+    dev = prob.to(DEV)
+    a = run_gpu(dev, out_dtype=torch.float32, debug_flags=atlas.DEBUG_TC_DIRECT)
+    b = run_gpu(dev, out_dtype=torch.float32, debug_flags=atlas.DEBUG_TC_DIRECT)
+    assert torch.equal(a, b)
+    perm = torch.randperm(prob.num_pages, generator=torch.Generator().manual_seed(3))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(prob.num_pages)
+    k2 = torch.empty_like(prob.k_pages)
+    v2 = torch.empty_like(prob.v_pages)
+    k2[inv] = prob.k_pages
+    v2[inv] = prob.v_pages
+    prob2 = inputs.Problem(**{**prob.__dict__, "k_pages": k2, "v_pages": v2,
+                              "page_table": inv[prob.page_table.long()].to(torch.int32)})
+    c = run_gpu(prob2.to(DEV), out_dtype=torch.float32, debug_flags=atlas.DEBUG_TC_DIRECT)
+    assert torch.equal(a, c)
+
+
+@pytest.mark.parametrize("flags,split", [(atlas.DEBUG_TC_DIRECT, 0), (0, 256)])
+def test_tc_bad_page_and_seq_len(flags, split):
+    prob = inputs.make("suffix", 3, 32, 4, 128, 32, [300, 400, 500], q_len=16, seed=4)
+    prob.page_table[1, 2] = -3
+    prob.seq_lens[2] = 7  # fewer keys than query rows
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status, split_tokens=split,
+                  debug_flags=flags)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st & atlas.DEV_BAD_PAGE and st & atlas.DEV_BAD_SEQLEN
+    assert torch.isnan(out[1]).all() and torch.isnan(out[2]).all()
+    assert torch.isfinite(out[0]).all()
+
+
+def test_prefill_rejects_seq_len_different_from_q_len():
+    prob = inputs.make("prefill", 2, 8, 2, 128, 64, [256, 256], seed=5)
+    prob.seq_lens[1] = 255
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status,
+                  debug_flags=atlas.DEBUG_TC_DIRECT)
+    torch.cuda.synchronize()
+    assert int(status.item()) & atlas.DEV_BAD_SEQLEN
+    assert torch.isnan(out[1]).all() and torch.isfinite(out[0]).all()
+
+
+def sampled(prob, rows, out32, out16):
+    ref = oracle_rows(prob, rows=rows)
+    D = prob.head_dim
+    idx = torch.from_numpy(rows).to(DEV)
+    assert_parity(prob, out32.reshape(-1, D)[idx], ref, "f32 out")
+    assert_parity(prob, out16.reshape(-1, D)[idx], ref, "bf16 out")
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+    assert torch.isfinite(out32).all()
+
+
+def test_config4_suffix_full_size_sampled_rows():
+    prob = inputs.make_config(4)
+    dev = prob.to(DEV)
+    out16 = run_gpu(dev)
+    out32 = run_gpu(dev, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([rng.choice(flat_rows(prob), 96, replace=False),
+                                     [0, 15, flat_rows(prob) - 1]]))
+    sampled(prob, rows, out32, out16)
+
+
+def test_config5_prefill_full_size_sampled_rows():
+    prob = inputs.make_config(5)
+    dev = prob.to(DEV)
+    out16 = run_gpu(dev)
+    out32 = run_gpu(dev, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    S, H = prob.q_len, prob.n_q_heads
+    rng = np.random.default_rng(5)
+    early = [(b * H + h) * S + i for b in range(2) for h in (0, 13, 31)
+             for i in (0, 1, 2, 63, 127, 128, 511, 512, 4095, S - 1)]
+    rows = np.unique(np.concatenate([rng.choice(flat_rows(prob), 64, replace=False), early]))
+    sampled(prob, rows, out32, out16)
