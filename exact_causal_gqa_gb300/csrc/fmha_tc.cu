@@ -57,7 +57,8 @@ enum {
     B_SFREE = B_SFULL + 2,
     B_PFULL = B_SFREE + 2,
     B_ODONE = B_PFULL + 1,
-    B_TAIL = B_ODONE + 1,
+    B_TAIL_READY = B_ODONE + 1,  // single use: the last V block has landed
+    B_TAIL = B_TAIL_READY + 1,   // single use: its rows past the last key are zeroed
     B_FINAL = B_TAIL + 1,
     NUM_BARS = B_FINAL + 1
 };
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mbar_init(BAR(B_PFULL), BM);
         mbar_init(BAR(B_ODONE), 1);
+        mbar_init(BAR(B_TAIL_READY), 1);
         mbar_init(BAR(B_TAIL), 1);
         mbar_init(BAR(B_FINAL), 1);
         *abort_flag = 0;
@@ -292,11 +294,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int s = j % KV_STAGES;
                 if (!mbar_wait_bounded(BAR(B_PFULL), j & 1, abort_flag, kWaitLimitNs) ||
                     !mbar_wait_bounded(BAR(B_VFULL + s), (j / KV_STAGES) & 1, abort_flag,
-                                       kWaitLimitNs) ||
-                    (j == nb - 1 && tail_fix &&
-                     !mbar_wait_bounded(BAR(B_TAIL), 0, abort_flag, kWaitLimitNs))) {
+                                       kWaitLimitNs)) {
                     ok = false;
                     break;
+                }
+                if (j == nb - 1 && tail_fix) {
+                    // Hand the landed last V block to the fix-up warp and wait for it.
+                    // (Only this thread observes every phase of the V ring in order.)
+                    mbar_arrive(BAR(B_TAIL_READY));
+                    if (!mbar_wait_bounded(BAR(B_TAIL), 0, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 tc_fence_after();
                 const uint32_t vbase = sb + OFF_V + s * kTileBytes;
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // -------------------------------------------------------- tail fix-up
         if (tail_fix) {
             const int j = nb - 1, s = j % KV_STAGES;
-            if (wait_warp(BAR(B_VFULL + s), (j / KV_STAGES) & 1, abort_flag)) {
+            if (wait_warp(BAR(B_TAIL_READY), 0, abort_flag)) {
                 const uint32_t vbase = sb + OFF_V + s * kTileBytes;
                 for (int idx = lane; idx < (BN - tail_first) * 16; idx += 32) {
                     const int row = tail_first + idx / 16, q = idx % 16;
