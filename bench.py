@@ -80,11 +80,15 @@ def work_of(prob):
     return kv, flops
 
 
+KERNEL_SOURCES = {"split_bf16_kernel": "split_kv.cu", "split_f32_kernel": "split_kv.cu",
+                  "fmha_tc_kernel": "fmha_tc.cu"}
+
+
 def traffic_record(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
     kernel source is unchanged since it was captured; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = os.path.join(ROOT, "exact_causal_gqa_gb300", "csrc", "split_kv.cu")
+    src = os.path.join(ROOT, "exact_causal_gqa_gb300", "csrc", KERNEL_SOURCES[kernel])
     if not os.path.exists(path):
         return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -277,7 +281,16 @@ def run_atlas(args, world, rank, local):
         achieved = flops / (main_avg * 1e-3) / 1e12
         peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
         bound = "tensor"
-    kernel = "split_bf16_kernel" if prob.dtype == "bf16" else "split_f32_kernel"
+    tc_path = prob.dtype == "bf16" and prob.head_dim == 128 and \
+        prob.q_len * (prob.n_q_heads // prob.n_kv_heads) > 16
+    if tc_path:
+        kernel = "fmha_tc_kernel"
+    else:
+        kernel = "split_bf16_kernel" if prob.dtype == "bf16" else "split_f32_kernel"
+    # launches per step: the main kernel, plus the merge unless the tensor-core
+    # path wrote the output directly (timer event 2 then coincides with event 1)
+    merge_ms = sum(t.merge_ms() for t in timers) / len(timers)
+    launches_per_step = 1 if (tc_path and ws_bytes == 0) else 2  # no workspace: no merge
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -305,6 +318,7 @@ def run_atlas(args, world, rank, local):
             "per_step_ms": {"min": round(min(step_ms), 5),
                             "median": round(statistics.median(step_ms), 5)},
             "main_kernel_ms": round(main_avg, 5),
+            "merge_kernel_ms": round(merge_ms, 5),
             "wall_s": round(wall, 4),
         },
         "roofline": {
@@ -317,7 +331,7 @@ def run_atlas(args, world, rank, local):
             "frac": round(achieved / peak, 4),
             "traffic": traffic_record(kernel, cfg["name"]),
         },
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "device_status": status_val,
     }
     # Samples of the timed region; if it was shorter than the 200 ms period, the

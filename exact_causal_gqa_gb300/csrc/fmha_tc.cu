@@ -381,31 +381,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(BAR(B_SFREE + sbuf));
 
             const int nvis = lim_row - (kv_begin + j * BN);  // visible columns of this row
-            float mx = -INFINITY;
+            // Scores in log2 units; eight independent max chains keep the pipes busy.
+            float mx8[8];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
+            for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+            if (__all_sync(0xffffffffu, nvis >= BN)) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float v = (cc * 32 + e) < nvis ? __uint_as_float(sr[cc][e]) * p.scale_log2
-                                                         : -INFINITY;
-                    sr[cc][e] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
-                }
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float v = __uint_as_float(sr[cc][e]) * p.scale_log2;
+                        sr[cc][e] = __float_as_uint(v);
+                        mx8[e & 7] = fmaxf(mx8[e & 7], v);
+                    }
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float v = (cc * 32 + e) < nvis
+                                            ? __uint_as_float(sr[cc][e]) * p.scale_log2
+                                            : -INFINITY;
+                        sr[cc][e] = __float_as_uint(v);
+                        mx8[e & 7] = fmaxf(mx8[e & 7], v);
+                    }
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             float corr = 1.f;
             if (mx > m_used + kRescaleThreshold) {
                 corr = ex2(m_used - mx);  // 0 on the first visible block
                 m_used = mx;
             }
             const float mref = m_used == -INFINITY ? 0.f : m_used;
-            float rs = 0.f;
+            float rs8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const float pv = ex2(__uint_as_float(sr[cc][e]) - mref);
                     sr[cc][e] = __float_as_uint(pv);
-                    rs += pv;
+                    rs8[e & 7] += pv;
                 }
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l = l * corr + rs;
 
             // PV of the previous block must be done before O is rescaled or P rewritten.
