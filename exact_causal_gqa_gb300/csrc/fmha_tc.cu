@@ -1,27 +1,32 @@
 // fmha_tc.cu -- causal prefill and suffix-query attention on the 5th-generation
 // tensor cores (tcgen05 + TMEM), fed by TMA from the page pool.
 //
-// One CTA owns a 128-row query tile of one (sequence, kv head): rows are the
-// G*q_len (q head, query row) pairs of the GQA group in memory order, so a tile
-// is one q head's 128 consecutive prompt rows (prefill) or all G heads x SQ rows
-// (suffix, G*SQ = 128).  It walks 128-key blocks up to the last key any of its
-// rows may see -- blocks past that are never loaded (the causal block skip of
-// the CPUAttn README, "Parallel lowerings") -- and folds each block into a
-// per-row online-softmax state, the page fold of the CFR-Atlas README.
+// A CTA owns NT (1 or 2) 128-row query tiles of one (sequence, kv head).  Tile
+// rows are the G*q_len (q head, query row) pairs of the GQA group in memory
+// order: one q head's 128 consecutive prompt rows (prefill) or all G heads x SQ
+// rows (suffix, G*SQ = 128).  With NT = 2 the two tiles are two q heads of the
+// same group at the same prompt rows, so they need exactly the same K/V blocks:
+// each block is loaded once for both, and the tensor core works on one tile
+// while the other tile's softmax runs.  The CTA walks 128-key blocks up to the
+// last key any of its rows may see -- later blocks are never loaded (causal
+// block skipping, CPUAttn README: the fused QK -> RowNorm -> PV tile pipeline
+// stops at the last reachable K block) -- and folds each block into per-row
+// online-softmax state (the page fold of the CFR-Atlas README, "Core contract").
 //
-// Warp roles (256 threads, one CTA per SM):
-//   warp 0      TMA producer: the Q tile once, then K and V blocks gathered page
-//               by page through the page table into a 2-stage ring.
-//   warp 1      allocates TMEM; one lane issues the MMAs:
-//                 S_j  = Q K_j^T  (M=128, N=128, K=128) into TMEM buffer j%2
-//                 O   += P_j V_j  (M=128, N=128, K=128) into TMEM, P from smem
-//   warp 2      zeroes V rows past the last key of the final block (they may be
-//               NaN-poisoned or stale, and 0 * NaN would reach O).
-//   warps 4-7   softmax: one thread per query row reads its S row from TMEM,
-//               masks, takes the row max, exponentiates (ex2), accumulates l,
-//               rescales O in TMEM when its max grew by more than 2^8, and writes
-//               P (bf16; plus the bf16 remainder P - bf16(P) for tiles whose rows
-//               see few keys) into smem for the PV product.  Epilogue: O / l.
+// Warp roles (128 + NT*128 threads, one CTA per SM):
+//   warp 0    TMA producer: the Q tiles once, then K and V blocks gathered page
+//             by page through the page table into a KV_STAGES-deep ring.
+//   warp 1    allocates TMEM; one lane issues the MMAs:
+//               S  = Q K^T  (M=128, N=128, K=128; A and B from smem)  -> TMEM
+//               O += P V    (M=128, N=128, K=128; A = P from TMEM, B = V from smem)
+//   warp 2    zeroes V rows past the last key of the final block (they may be
+//             NaN-poisoned or stale, and 0 * NaN would reach O).
+//   warps 4+  one softmax warpgroup per tile, one thread per query row: read the
+//             S row from TMEM, mask, row max, ex2, row sum; rescale O in TMEM
+//             when the row max grew by more than 2^8 (exact: acc and l always
+//             share the reference max); write P as bf16 over its own S columns
+//             (plus the bf16 remainder P - bf16(P) for tiles whose rows see few
+//             keys, so that PV keeps ~16 bits of P there).  Epilogue: O / l.
 // Every mbarrier wait is bounded; a CTA that gives up records ATLAS_DEV_TIMEOUT,
 // lets its copies and MMAs finish, frees TMEM and writes NaN.
 #include "internal.h"
@@ -29,59 +34,92 @@
 
 #include <math.h>
 
+// Compile-time timeline hooks for profiling builds (-DATLAS_TRACE): one CTA
+// records (clock64, role, event, block) tuples into a device array that the
+// profiling build reads back.  Compiled out of the library.
+#ifdef ATLAS_TRACE
+__device__ unsigned long long g_atlas_trace[8 * 16 * 512];  // [role][event][block]
+__device__ int g_atlas_trace_cta;
+#define TRACE(role, ev, j)                                                             \
+    do {                                                                               \
+        if ((int)(blockIdx.x + blockIdx.y * gridDim.x) == g_atlas_trace_cta && (j) < 512) \
+            g_atlas_trace[((role) * 16 + (ev)) * 512 + (j)] = clock64();               \
+    } while (0)
+extern "C" int atlas_trace_read(unsigned long long *host, int cta) {
+    if (host) cudaMemcpyFromSymbol(host, g_atlas_trace, sizeof(g_atlas_trace));
+    static unsigned long long zeros[8 * 16 * 512];
+    cudaMemcpyToSymbol(g_atlas_trace, zeros, sizeof(zeros));
+    cudaMemcpyToSymbol(g_atlas_trace_cta, &cta, sizeof(cta));
+    return 0;
+}
+#else
+#define TRACE(role, ev, j) \
+    do {                   \
+    } while (0)
+#endif
+
 namespace atlas {
 namespace {
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per block
-constexpr int KV_STAGES = 2;
-constexpr int kTcThreads = 256;
-constexpr int kTileBytes = 128 * 128 * 2;  // a 128 x 128 bf16 tile (Q, K, V or P)
+constexpr int kTileBytes = 128 * 128 * 2;  // a 128 x 128 bf16 tile (Q, K or V)
 constexpr int kSlab = 128 * 128;           // one 64-column slab of such a tile
-
-constexpr int OFF_Q = 0;
-constexpr int OFF_P = OFF_Q + kTileBytes;
-constexpr int OFF_PL = OFF_P + kTileBytes;
-// V stages sit below K stages: the PV product's MN-major B descriptor strides by
-// a 16 KB slab, and every address it can form stays inside the CTA's allocation.
-constexpr int OFF_V = OFF_PL + kTileBytes;
-constexpr int OFF_K = OFF_V + KV_STAGES * kTileBytes;
-constexpr int OFF_BAR = OFF_K + KV_STAGES * kTileBytes;
-enum {
-    B_Q = 0,
-    B_KFULL = 1,
-    B_KEMPTY = B_KFULL + KV_STAGES,
-    B_VFULL = B_KEMPTY + KV_STAGES,
-    B_VEMPTY = B_VFULL + KV_STAGES,
-    B_SFULL = B_VEMPTY + KV_STAGES,
-    B_SFREE = B_SFULL + 2,
-    B_PFULL = B_SFREE + 2,
-    B_ODONE = B_PFULL + 1,
-    B_TAIL_READY = B_ODONE + 1,  // single use: the last V block has landed
-    B_TAIL = B_TAIL_READY + 1,   // single use: its rows past the last key are zeroed
-    B_FINAL = B_TAIL + 1,
-    NUM_BARS = B_FINAL + 1
-};
-constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_FLAG = OFF_TMEM + 8;
-constexpr int kTcSmem = OFF_FLAG + 8 + 1024;  // + slack to align the base to 1024 B
-static_assert(kTcSmem <= 232448, "shared memory budget");
-
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_S = 0;    // two S buffers: columns [0,128) and [128,256)
-constexpr uint32_t TM_O = 256;  // O accumulator: columns [256,384)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows 256x
+
+template <int NT>
+struct Cfg {
+    static constexpr int kStages = NT == 2 ? 2 : 3;  // K/V ring depth
+    static constexpr int kSB = NT == 2 ? 1 : 2;      // S buffers per tile
+    // warps 0-2: producer, MMA issuer, tail fix-up (warp 3 idle); then NT softmax
+    // warpgroups.  Each SMSP holds 16K registers and 3 of the 12 warps (NT = 2):
+    // 168 registers per thread.
+    static constexpr int kSoftmaxWarp0 = 4;
+    static constexpr int kThreads = 32 * kSoftmaxWarp0 + NT * 128;
+    static constexpr int OFF_Q = 0;
+    // V stages below K stages: the PV product's MN-major B descriptor strides by a
+    // 16 KB slab, and every address it can form stays inside the allocation.
+    static constexpr int OFF_V = OFF_Q + NT * kTileBytes;
+    static constexpr int OFF_K = OFF_V + kStages * kTileBytes;
+    static constexpr int OFF_BAR = OFF_K + kStages * kTileBytes;
+    // barrier indices
+    static constexpr int B_Q = 0;
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_KEMPTY = B_KFULL + kStages;
+    static constexpr int B_VFULL = B_KEMPTY + kStages;
+    static constexpr int B_VEMPTY = B_VFULL + kStages;
+    static constexpr int B_SFULL = B_VEMPTY + kStages;  // [NT][kSB]
+    static constexpr int B_PFULL = B_SFULL + NT * kSB;  // [NT]
+    static constexpr int B_PVDONE = B_PFULL + NT;       // [NT]
+    static constexpr int B_TAIL_READY = B_PVDONE + NT;  // single use
+    static constexpr int B_TAIL = B_TAIL_READY + 1;     // single use
+    static constexpr int B_FINAL = B_TAIL + 1;
+    static constexpr int kBars = B_FINAL + 1;
+    static constexpr int OFF_TMEM = OFF_BAR + kBars * 8;
+    static constexpr int OFF_FLAG = OFF_TMEM + 8;
+    static constexpr int kSmem = OFF_FLAG + 8 + 1024;  // + slack to align the base
+    static_assert(kSmem <= 232448, "shared memory budget");
+    // TMEM columns: NT=2 -> [S0 | O0 | S1 | O1]; NT=1 -> [S(buf 0) | S(buf 1) | O]
+    __device__ static constexpr uint32_t s_col(int x, int b) {
+        return NT == 2 ? (uint32_t)x * 256u : (uint32_t)b * 128u;
+    }
+    __device__ static constexpr uint32_t o_col(int x) {
+        return NT == 2 ? (uint32_t)x * 256u + 128u : 256u;
+    }
+};
 
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort) {
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort, kWaitLimitNs));
 }
 
-// Writes NaN to the rows of this tile (direct mode) -- used when the tile's
-// sequence or pages are invalid, or a wait gave up.
-__device__ void nan_rows(const TcParams &p, int b, int hkv, int f0, int rows_unit, int r) {
-    const int f = f0 + r;
-    if (f >= rows_unit) return;
-    const int64_t row = ((int64_t)b * p.Hq + (int64_t)hkv * p.G) * p.q_len + f;
+__device__ __forceinline__ int64_t tile_row(const TcParams &p, int b, int hkv, int f) {
+    return ((int64_t)b * p.Hq + (int64_t)hkv * p.G) * p.q_len + f;
+}
+
+// NaN for row f of (b, hkv) in direct mode.
+__device__ void nan_row(const TcParams &p, int b, int hkv, int f) {
+    const int64_t row = tile_row(p, b, hkv, f);
     const float nan = __int_as_float(0x7fc00000);
     if (p.out_bf16) {
         uint4 v;
@@ -95,42 +133,51 @@ __device__ void nan_rows(const TcParams &p, int b, int hkv, int f0, int rows_uni
     if (p.lse) p.lse[row] = nan;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int NT>
+__global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+    using C = Cfg<NT>;
+    constexpr int S = C::kStages, SB = C::kSB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#define BAR(i) (sb + OFF_BAR + 8u * (uint32_t)(i))
+#define BAR(i) (sb + C::OFF_BAR + 8u * (uint32_t)(i))
 
     // ------------------------------------------------------------ work item
     const int units = p.B * p.Hkv;
-    int u, t, c;
+    int u, c, t0, tstep;  // tiles t0 + x * tstep, x < NT
     if (p.split) {
         c = blockIdx.x;
         u = blockIdx.y / p.tiles_per_unit;
-        t = blockIdx.y % p.tiles_per_unit;
+        t0 = blockIdx.y % p.tiles_per_unit;
+        tstep = 0;
     } else {
         c = 0;
         const int r = blockIdx.x;
         if (p.tiles_per_head > 0) {  // heavy tiles (late prompt rows) first
-            const int per = units * p.G;
+            const int heads = p.G / NT;  // head groups of NT heads
+            const int per = units * heads;
             const int rest = r % per;
-            u = rest / p.G;
-            t = (rest % p.G) * p.tiles_per_head + (p.tiles_per_head - 1 - r / per);
+            u = rest / heads;
+            const int qi = p.tiles_per_head - 1 - r / per;
+            t0 = (rest % heads) * NT * p.tiles_per_head + qi;
+            tstep = p.tiles_per_head;
         } else {
             u = r % units;
-            t = r / units;
+            t0 = r / units;
+            tstep = 0;
         }
     }
     const int b = u / p.Hkv, hkv = u % p.Hkv;
     const int L = p.seq_lens[b];
     const int rows_unit = p.G * p.q_len;
-    const int f0 = t * BM;
+    // Both tiles cover the same prompt rows, so their key ranges agree.
+    const int f0 = t0 * BM;
     const int f_last = min(f0 + BM, rows_unit) - 1;
     const bool spans = (f_last / p.q_len) != (f0 / p.q_len);
     const int i_max = spans ? p.q_len - 1 : f_last % p.q_len;
@@ -138,11 +185,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (L < p.q_len || L > p.max_pages * p.P || (p.require_full && L != p.q_len)) {
         if (threadIdx.x == 0 && c == 0 && p.status) atomicOr(p.status, ATLAS_DEV_BAD_SEQLEN);
-        if (!p.split && threadIdx.x < BM) nan_rows(p, b, hkv, f0, rows_unit, threadIdx.x);
+        if (!p.split && threadIdx.x < NT * BM) {
+            const int f = (t0 + (int)(threadIdx.x / BM) * tstep) * BM + threadIdx.x % BM;
+            if (f < rows_unit) nan_row(p, b, hkv, f);
+        }
         return;  // split mode: the merge writes NaN rows for this sequence
     }
-    const int kv_hi = L - p.q_len + i_max + 1;   // keys the tile's last row sees
-    const int kv_min = L - p.q_len + i_min + 1;  // keys its first row sees
+    const int kv_hi = L - p.q_len + i_max + 1;   // keys the tiles' last row sees
+    const int kv_min = L - p.q_len + i_min + 1;  // keys their first row sees
     int kv_begin = 0, kv_end = kv_hi;
     if (p.split) {
         kv_begin = c * p.chunk;
@@ -159,14 +209,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (__syncthreads_or(bad)) {
             if (threadIdx.x == 0 && p.status) atomicOr(p.status, ATLAS_DEV_BAD_PAGE);
-            if (threadIdx.x < BM) {
-                if (!p.split) {
-                    nan_rows(p, b, hkv, f0, rows_unit, threadIdx.x);
-                } else if (f0 + (int)threadIdx.x < rows_unit) {
-                    const int64_t row =
-                        ((int64_t)b * p.Hq + (int64_t)hkv * p.G) * p.q_len + f0 + threadIdx.x;
-                    float *ml = p.ws_ml + (row * p.n_chunks + c) * 2;
-                    ml[0] = ml[1] = __int_as_float(0x7fc00000);
+            if (threadIdx.x < NT * BM) {
+                const int f = (t0 + (int)(threadIdx.x / BM) * tstep) * BM + threadIdx.x % BM;
+                if (f < rows_unit) {
+                    if (!p.split) {
+                        nan_row(p, b, hkv, f);
+                    } else {
+                        float *ml = p.ws_ml + (tile_row(p, b, hkv, f) * p.n_chunks + c) * 2;
+                        ml[0] = ml[1] = __int_as_float(0x7fc00000);
+                    }
                 }
             }
             return;
@@ -179,22 +230,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
-        mbar_init(BAR(B_Q), 1);
-        for (int s = 0; s < KV_STAGES; ++s) {
-            mbar_init(BAR(B_KFULL + s), 1);
-            mbar_init(BAR(B_KEMPTY + s), 1);
-            mbar_init(BAR(B_VFULL + s), 1);
-            mbar_init(BAR(B_VEMPTY + s), 1);
+        mbar_init(BAR(C::B_Q), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(BAR(C::B_KFULL + s), 1);
+            mbar_init(BAR(C::B_KEMPTY + s), 1);
+            mbar_init(BAR(C::B_VFULL + s), 1);
+            mbar_init(BAR(C::B_VEMPTY + s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(BAR(B_SFULL + s), 1);
-            mbar_init(BAR(B_SFREE + s), BM);
+        for (int k = 0; k < NT * SB; ++k) mbar_init(BAR(C::B_SFULL + k), 1);
+        for (int x = 0; x < NT; ++x) {
+            mbar_init(BAR(C::B_PFULL + x), BM);
+            mbar_init(BAR(C::B_PVDONE + x), 1);
         }
-        mbar_init(BAR(B_PFULL), BM);
-        mbar_init(BAR(B_ODONE), 1);
-        mbar_init(BAR(B_TAIL_READY), 1);
-        mbar_init(BAR(B_TAIL), 1);
-        mbar_init(BAR(B_FINAL), 1);
+        mbar_init(BAR(C::B_TAIL_READY), 1);
+        mbar_init(BAR(C::B_TAIL), 1);
+        mbar_init(BAR(C::B_FINAL), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -211,28 +261,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            const int qrow = (b * p.Hq + hkv * p.G) * p.q_len + f0;
-            mbar_arrive_expect_tx(BAR(B_Q), kTileBytes);
-            tma_load_2d(sb + OFF_Q, &tmQ, 0, qrow, BAR(B_Q));
-            tma_load_2d(sb + OFF_Q + kSlab, &tmQ, 64, qrow, BAR(B_Q));
+            mbar_arrive_expect_tx(BAR(C::B_Q), NT * kTileBytes);
+            for (int x = 0; x < NT; ++x) {
+                const int qrow = (int)tile_row(p, b, hkv, (t0 + x * tstep) * BM);
+                tma_load_2d(sb + C::OFF_Q + x * kTileBytes, &tmQ, 0, qrow, BAR(C::B_Q));
+                tma_load_2d(sb + C::OFF_Q + x * kTileBytes + kSlab, &tmQ, 64, qrow, BAR(C::B_Q));
+            }
             const int BR = p.P < BN ? p.P : BN;
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < nb && !failed; ++j) {
-                const int s = j % KV_STAGES, use = j / KV_STAGES;
+                const int s = j % S, use = j / S;
                 const int kb = kv_begin + j * BN;
                 const int ke = min(kb + BN, kv_end);
                 const int nbox = (ke - kb + BR - 1) / BR;
                 const uint32_t bytes = (uint32_t)(nbox * BR * 128 * 2);
                 for (int kv = 0; kv < 2; ++kv) {
-                    const int full = (kv == 0 ? B_KFULL : B_VFULL) + s;
-                    const int empty = (kv == 0 ? B_KEMPTY : B_VEMPTY) + s;
+                    const int full = (kv == 0 ? C::B_KFULL : C::B_VFULL) + s;
+                    const int empty = (kv == 0 ? C::B_KEMPTY : C::B_VEMPTY) + s;
                     if (use > 0 &&
                         !mbar_wait_bounded(BAR(empty), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
                         failed = true;
                         break;
                     }
                     const CUtensorMap *map = kv == 0 ? &tmK : &tmV;
-                    const uint32_t dst = sb + (kv == 0 ? OFF_K : OFF_V) + s * kTileBytes;
+                    const uint32_t dst = sb + (kv == 0 ? C::OFF_K : C::OFF_V) + s * kTileBytes;
                     mbar_arrive_expect_tx(BAR(full), bytes);
                     for (int bx = 0; bx < nbox; ++bx) {
                         const int tk = kb + bx * BR;
@@ -243,18 +295,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     if (kv == 0) issued_k = j + 1;
                     else issued_v = j + 1;
+                    TRACE(0, kv, j);
                 }
             }
             if (failed) {
                 *abort_flag = 1;
                 int no_abort = 0;
-                mbar_wait_bounded(BAR(B_Q), 0, &no_abort, kWaitLimitNs);
-                for (int j = max(0, issued_k - KV_STAGES); j < issued_k; ++j)
-                    mbar_wait_bounded(BAR(B_KFULL + j % KV_STAGES), (j / KV_STAGES) & 1, &no_abort,
-                                      kWaitLimitNs);
-                for (int j = max(0, issued_v - KV_STAGES); j < issued_v; ++j)
-                    mbar_wait_bounded(BAR(B_VFULL + j % KV_STAGES), (j / KV_STAGES) & 1, &no_abort,
-                                      kWaitLimitNs);
+                mbar_wait_bounded(BAR(C::B_Q), 0, &no_abort, kWaitLimitNs);
+                for (int j = max(0, issued_k - S); j < issued_k; ++j)
+                    mbar_wait_bounded(BAR(C::B_KFULL + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
+                for (int j = max(0, issued_v - S); j < issued_v; ++j)
+                    mbar_wait_bounded(BAR(C::B_VFULL + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
             }
         }
         __syncwarp();
@@ -263,86 +314,107 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false);
             constexpr uint32_t idPV = idesc_bf16_f32(128, 128, true);
-            bool ok = mbar_wait_bounded(BAR(B_Q), 0, abort_flag, kWaitLimitNs);
+            bool ok = mbar_wait_bounded(BAR(C::B_Q), 0, abort_flag, kWaitLimitNs);
             tc_fence_after();
+            // S_x(j) = Q_x K_j^T for every tile into S buffer j % SB.
             auto issue_s = [&](int j) -> bool {
-                const int s = j % KV_STAGES, sbuf = j & 1;
-                if (!mbar_wait_bounded(BAR(B_KFULL + s), (j / KV_STAGES) & 1, abort_flag,
-                                       kWaitLimitNs))
-                    return false;
-                if (j >= 2 && !mbar_wait_bounded(BAR(B_SFREE + sbuf), ((j >> 1) - 1) & 1,
-                                                 abort_flag, kWaitLimitNs))
+                const int s = j % S;
+                if (!mbar_wait_bounded(BAR(C::B_KFULL + s), (j / S) & 1, abort_flag, kWaitLimitNs))
                     return false;
                 tc_fence_after();
-                const uint32_t kbase = sb + OFF_K + s * kTileBytes;
+                const uint32_t kbase = sb + C::OFF_K + s * kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-                    umma_bf16(tmem + TM_S + sbuf * 128, sdesc_sw128(sb + OFF_Q + off, 16, 1024),
-                              sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0);
+                for (int x = 0; x < NT; ++x) {
+                    const uint32_t qbase = sb + C::OFF_Q + x * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
+                        umma_bf16(tmem + C::s_col(x, j % SB), sdesc_sw128(qbase + off, 16, 1024),
+                                  sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0);
+                    }
+                    umma_commit(BAR(C::B_SFULL + x * SB + j % SB));
                 }
-                umma_commit(BAR(B_SFULL + sbuf));
-                umma_commit(BAR(B_KEMPTY + s));
+                umma_commit(BAR(C::B_KEMPTY + s));
+                TRACE(1, 1, j);
                 return true;
             };
-            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < min(SB, nb); ++j) ok = issue_s(j);
             for (int j = 0; ok && j < nb; ++j) {
-                if (j + 1 < nb && !issue_s(j + 1)) {
-                    ok = false;
-                    break;
-                }
-                const int s = j % KV_STAGES;
-                if (!mbar_wait_bounded(BAR(B_PFULL), j & 1, abort_flag, kWaitLimitNs) ||
-                    !mbar_wait_bounded(BAR(B_VFULL + s), (j / KV_STAGES) & 1, abort_flag,
-                                       kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                if (j == nb - 1 && tail_fix) {
-                    // Hand the landed last V block to the fix-up warp and wait for it.
-                    // (Only this thread observes every phase of the V ring in order.)
-                    mbar_arrive(BAR(B_TAIL_READY));
-                    if (!mbar_wait_bounded(BAR(B_TAIL), 0, abort_flag, kWaitLimitNs)) {
+                const int s = j % S;
+#pragma unroll
+                for (int x = 0; x < NT; ++x) {
+                    TRACE(1, 2 + 16 * x, j);
+                    if (!mbar_wait_bounded(BAR(C::B_PFULL + x), j & 1, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                }
-                tc_fence_after();
-                const uint32_t vbase = sb + OFF_V + s * kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t aoff = (kk >> 2) * kSlab + (kk & 3) * 32;
-                    umma_bf16(tmem + TM_O, sdesc_sw128(sb + OFF_P + aoff, 16, 1024),
-                              sdesc_sw128(vbase + kk * 2048, kSlab, 1024), idPV,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                if (hilo) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t aoff = (kk >> 2) * kSlab + (kk & 3) * 32;
-                        umma_bf16(tmem + TM_O, sdesc_sw128(sb + OFF_PL + aoff, 16, 1024),
-                                  sdesc_sw128(vbase + kk * 2048, kSlab, 1024), idPV, 1u);
+                    TRACE(1, 3 + 16 * x, j);
+                    if (x == 0) {
+                        if (!mbar_wait_bounded(BAR(C::B_VFULL + s), (j / S) & 1, abort_flag,
+                                               kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        if (j == nb - 1 && tail_fix) {
+                            // Hand the landed last V block to the fix-up warp (only this
+                            // thread observes every phase of the V ring in order).
+                            mbar_arrive(BAR(C::B_TAIL_READY));
+                            if (!mbar_wait_bounded(BAR(C::B_TAIL), 0, abort_flag, kWaitLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                        }
                     }
+                    tc_fence_after();
+                    const uint32_t vbase = sb + C::OFF_V + s * kTileBytes;
+                    const uint32_t pcol = tmem + C::s_col(x, j % SB);
+                    // keys 16kk .. 16kk+15 of P sit in columns (kk/4)*64 + (kk%4)*8 .. +8;
+                    // their remainders 32 columns further on.
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16_tmem_a(tmem + C::o_col(x), pcol + (kk >> 2) * 64 + (kk & 3) * 8,
+                                         sdesc_sw128(vbase + kk * 2048, kSlab, 1024), idPV,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                    if (hilo) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_bf16_tmem_a(tmem + C::o_col(x),
+                                             pcol + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
+                                             sdesc_sw128(vbase + kk * 2048, kSlab, 1024), idPV, 1u);
+                    }
+                    umma_commit(BAR(C::B_PVDONE + x));
+                    TRACE(1, 4 + 16 * x, j);
                 }
-                umma_commit(BAR(B_ODONE));
-                umma_commit(BAR(B_VEMPTY + s));
+                if (!ok) break;
+                umma_commit(BAR(C::B_VEMPTY + s));
+                const int jn = j + SB;
+                if (jn < nb) {
+                    // S buffer jn % SB holds P_x(j) until PV_x(j) has run.
+#pragma unroll
+                    for (int x = 0; x < NT; ++x)
+                        if (ok && !mbar_wait_bounded(BAR(C::B_PVDONE + x), j & 1, abort_flag,
+                                                     kWaitLimitNs))
+                            ok = false;
+                    TRACE(1, 5, j);
+                    if (ok) ok = issue_s(jn);
+                }
             }
             if (!ok) {
                 failed = true;
                 *abort_flag = 1;
             }
             // Every MMA issued so far completes before TMEM is released.
-            umma_commit(BAR(B_FINAL));
+            umma_commit(BAR(C::B_FINAL));
             int no_abort = 0;
-            mbar_wait_bounded(BAR(B_FINAL), 0, &no_abort, kWaitLimitNs);
+            mbar_wait_bounded(BAR(C::B_FINAL), 0, &no_abort, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 2) {
         // -------------------------------------------------------- tail fix-up
         if (tail_fix) {
-            const int j = nb - 1, s = j % KV_STAGES;
-            if (wait_warp(BAR(B_TAIL_READY), 0, abort_flag)) {
-                const uint32_t vbase = sb + OFF_V + s * kTileBytes;
+            const int s = (nb - 1) % S;
+            if (wait_warp(BAR(C::B_TAIL_READY), 0, abort_flag)) {
+                const uint32_t vbase = sb + C::OFF_V + s * kTileBytes;
                 for (int idx = lane; idx < (BN - tail_first) * 16; idx += 32) {
                     const int row = tail_first + idx / 16, q = idx % 16;
                     st_shared_v4(vbase + (q / 8) * kSlab + row * 128 + (q % 8) * 16, 0u, 0u, 0u,
@@ -350,59 +422,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(B_TAIL));
+                if (lane == 0) mbar_arrive(BAR(C::B_TAIL));
             } else {
                 failed = true;
             }
         }
-    } else if (warp >= 4) {
+    } else if (warp >= C::kSoftmaxWarp0) {
         // -------------------------------------------------------- softmax
-        const int q4 = warp - 4;
+        // Four consecutive warps cover the four TMEM lane quadrants (warp % 4).
+        const int x = (warp - C::kSoftmaxWarp0) / 4;  // tile of this warpgroup
+        const int q4 = warp % 4;                      // TMEM lane quadrant
         const int r = q4 * 32 + lane;
-        const int f = f0 + r;
+        const int f = (t0 + x * tstep) * BM + r;
         const bool valid = f < rows_unit;
         const int i = valid ? f % p.q_len : 0;
         const int lim_row = valid ? min(L - p.q_len + i + 1, kv_end) : 0;
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+        const uint32_t to = tl + C::o_col(x);
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
-            const int sbuf = j & 1;
-            if (!wait_warp(BAR(B_SFULL + sbuf), (j >> 1) & 1, abort_flag)) {
+            const int bsel = j % SB;
+            if (r == 0) TRACE(2 + x, 1, j);
+            if (!wait_warp(BAR(C::B_SFULL + x * SB + bsel), (j / SB) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
+            if (r == 0) TRACE(2 + x, 2, j);
             tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tl + TM_S + sbuf * 128 + cc * 32, sr[cc]);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(BAR(B_SFREE + sbuf));
-
+            const uint32_t ts = tl + C::s_col(x, bsel);
             const int nvis = lim_row - (kv_begin + j * BN);  // visible columns of this row
-            // Scores in log2 units; eight independent max chains keep the pipes busy.
+            const bool all_visible = __all_sync(0xffffffffu, nvis >= BN);
+            // Pass 1: row max of the scores (log2 units), eight independent chains.
+            // Outer loops stay rolled: the fully unrolled body overflows the
+            // instruction cache shared with the producer and MMA warps.
             float mx8[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-            if (__all_sync(0xffffffffu, nvis >= BN)) {
+#pragma unroll 1
+            for (int cc = 0; cc < 4; cc += 2) {
+                uint32_t sr[2][32];
+                tmem_ld32(ts + cc * 32, sr[0]);
+                tmem_ld32(ts + cc * 32 + 32, sr[1]);
+                tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float v = __uint_as_float(sr[cc][e]) * p.scale_log2;
-                        sr[cc][e] = __float_as_uint(v);
-                        mx8[e & 7] = fmaxf(mx8[e & 7], v);
-                    }
-            } else {
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
+                for (int q = 0; q < 2; ++q)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float v = (cc * 32 + e) < nvis
-                                            ? __uint_as_float(sr[cc][e]) * p.scale_log2
+                        const float v = (all_visible || (cc + q) * 32 + e < nvis)
+                                            ? __uint_as_float(sr[q][e]) * p.scale_log2
                                             : -INFINITY;
-                        sr[cc][e] = __float_as_uint(v);
                         mx8[e & 7] = fmaxf(mx8[e & 7], v);
                     }
             }
@@ -414,124 +483,137 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 m_used = mx;
             }
             const float mref = m_used == -INFINITY ? 0.f : m_used;
-            float rs8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float pv = ex2(__uint_as_float(sr[cc][e]) - mref);
-                    sr[cc][e] = __float_as_uint(pv);
-                    rs8[e & 7] += pv;
-                }
-            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
-                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-            l = l * corr + rs;
+            if (r == 0) TRACE(2 + x, 3, j + 0 * (int)(mref != mref));
 
-            // PV of the previous block must be done before O is rescaled or P rewritten.
-            if (j > 0 && !wait_warp(BAR(B_ODONE), (j - 1) & 1, abort_flag)) {
+            // O must hold PV(j-1) before it is rescaled.  With one S buffer the
+            // MMA issued S(j) only after PV(j-1) completed, so S being full says so.
+            if (SB > 1 && j > 0 && !wait_warp(BAR(C::B_PVDONE + x), (j - 1) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tl + TM_O + cc * 32, o);
+                    tmem_ld32(to + cc * 32, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-                    tmem_st32(tl + TM_O + cc * 32, o);
+                    tmem_st32(to + cc * 32, o);
                 }
-                tmem_wait_st();
             }
-            // P row r into the K-major, 128-byte-swizzled A tile (and its remainder).
+            // Pass 2, one half (64 keys) at a time: P = 2^(s - m) as bf16 pairs
+            // written over columns of S already read -- keys 64h .. 64h+63 go to
+            // columns 64h .. 64h+31 (keys 2k, 2k+1 in one column) and, when
+            // requested, their remainders P - bf16(P) to columns 64h+32 .. 64h+63.
+            float rs8[8];
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const int cc = ch / 4, e0 = (ch % 4) * 8;
-                uint32_t hw[4], lw[4];
+            for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
+            if (r == 0) TRACE(2 + x, 5, j);
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sr[2][32];
+                tmem_ld32(ts + h * 64, sr[0]);
+                tmem_ld32(ts + h * 64 + 32, sr[1]);
+                tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float a = __uint_as_float(sr[cc][e0 + 2 * k]);
-                    const float bb = __uint_as_float(sr[cc][e0 + 2 * k + 1]);
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
-                    hw[k] = *reinterpret_cast<const uint32_t *>(&h);
-                    if (hilo) {
-                        const float2 hf = __bfloat1622float2(h);
-                        lw[k] = pack_bf16(a - hf.x, bb - hf.y);
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t hw[16], lw[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int c0 = h * 64 + q * 32 + 2 * k;
+                        const float s0 = __uint_as_float(sr[q][2 * k]) * p.scale_log2;
+                        const float s1 = __uint_as_float(sr[q][2 * k + 1]) * p.scale_log2;
+                        const float a = (all_visible || c0 < nvis) ? ex2(s0 - mref) : 0.f;
+                        const float bb = (all_visible || c0 + 1 < nvis) ? ex2(s1 - mref) : 0.f;
+                        rs8[(2 * k) & 7] += a;
+                        rs8[(2 * k + 1) & 7] += bb;
+                        const __nv_bfloat162 hv = __floats2bfloat162_rn(a, bb);
+                        hw[k] = *reinterpret_cast<const uint32_t *>(&hv);
+                        if (hilo) {
+                            const float2 hf = __bfloat1622float2(hv);
+                            lw[k] = pack_bf16(a - hf.x, bb - hf.y);
+                        }
                     }
+                    tmem_st16(ts + h * 64 + q * 16, hw);
+                    if (hilo) tmem_st16(ts + h * 64 + 32 + q * 16, lw);
                 }
-                const uint32_t off = (ch / 8) * kSlab + sw128(r, ch % 8);
-                st_shared_v4(sb + OFF_P + off, hw[0], hw[1], hw[2], hw[3]);
-                if (hilo) st_shared_v4(sb + OFF_PL + off, lw[0], lw[1], lw[2], lw[3]);
             }
-            fence_proxy_async_smem();
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            l = l * corr + rs;
+            if (r == 0) TRACE(2 + x, 6, j + 0 * (int)(l != l));
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(B_PFULL));
+            mbar_arrive(BAR(C::B_PFULL + x));
+            if (r == 0) TRACE(2 + x, 4, j);
         }
-        if (ok && !wait_warp(BAR(B_ODONE), (nb - 1) & 1, abort_flag)) ok = false;
+        if (ok && !wait_warp(BAR(C::B_PVDONE + x), (nb - 1) & 1, abort_flag)) ok = false;
         if (!ok) {
             failed = true;
             *abort_flag = 1;
         }
         // ---------------------------------------------------- epilogue
         tc_fence_after();
-        uint32_t o[4][32];
         if (ok) {
+            const float inv = 1.f / l;
+            const int64_t row = tile_row(p, b, hkv, valid ? f : 0);
+            const int64_t slot = row * p.n_chunks + c;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(to + cc * 32, o);
+                tmem_wait_ld();
+                if (!valid) continue;
+                if (p.split) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + slot * 128 + cc * 32);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tl + TM_O + cc * 32, o[cc]);
-            tmem_wait_ld();
-        }
-        if (valid) {
-            const int64_t row = ((int64_t)b * p.Hq + (int64_t)hkv * p.G) * p.q_len + f;
-            if (p.split) {
-                const int64_t slot = row * p.n_chunks + c;
-                float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + slot * 128);
-                if (ok) {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[k / 8][(k % 8) * 4]),
-                                             __uint_as_float(o[k / 8][(k % 8) * 4 + 1]),
-                                             __uint_as_float(o[k / 8][(k % 8) * 4 + 2]),
-                                             __uint_as_float(o[k / 8][(k % 8) * 4 + 3]));
-                    p.ws_ml[slot * 2] = m_used;
-                    p.ws_ml[slot * 2 + 1] = l;
-                } else {
-                    p.ws_ml[slot * 2] = p.ws_ml[slot * 2 + 1] = __int_as_float(0x7fc00000);
-                }
-            } else if (ok) {
-                const float inv = 1.f / l;
-                if (p.out_bf16) {
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                             __uint_as_float(o[4 * k + 2]),
+                                             __uint_as_float(o[4 * k + 3]));
+                } else if (p.out_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                           row * 128);
+                                                           row * 128 + cc * 32);
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int cc = k / 4, e0 = (k % 4) * 8;
+                    for (int k = 0; k < 4; ++k) {
                         uint4 v;
-                        v.x = pack_bf16(__uint_as_float(o[cc][e0 + 0]) * inv,
-                                        __uint_as_float(o[cc][e0 + 1]) * inv);
-                        v.y = pack_bf16(__uint_as_float(o[cc][e0 + 2]) * inv,
-                                        __uint_as_float(o[cc][e0 + 3]) * inv);
-                        v.z = pack_bf16(__uint_as_float(o[cc][e0 + 4]) * inv,
-                                        __uint_as_float(o[cc][e0 + 5]) * inv);
-                        v.w = pack_bf16(__uint_as_float(o[cc][e0 + 6]) * inv,
-                                        __uint_as_float(o[cc][e0 + 7]) * inv);
+                        v.x = pack_bf16(__uint_as_float(o[8 * k + 0]) * inv,
+                                        __uint_as_float(o[8 * k + 1]) * inv);
+                        v.y = pack_bf16(__uint_as_float(o[8 * k + 2]) * inv,
+                                        __uint_as_float(o[8 * k + 3]) * inv);
+                        v.z = pack_bf16(__uint_as_float(o[8 * k + 4]) * inv,
+                                        __uint_as_float(o[8 * k + 5]) * inv);
+                        v.w = pack_bf16(__uint_as_float(o[8 * k + 6]) * inv,
+                                        __uint_as_float(o[8 * k + 7]) * inv);
                         dst[k] = v;
                     }
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * 128);
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
+                                                             row * 128 + cc * 32);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[k / 8][(k % 8) * 4]) * inv,
-                                             __uint_as_float(o[k / 8][(k % 8) * 4 + 1]) * inv,
-                                             __uint_as_float(o[k / 8][(k % 8) * 4 + 2]) * inv,
-                                             __uint_as_float(o[k / 8][(k % 8) * 4 + 3]) * inv);
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv,
+                                             __uint_as_float(o[4 * k + 1]) * inv,
+                                             __uint_as_float(o[4 * k + 2]) * inv,
+                                             __uint_as_float(o[4 * k + 3]) * inv);
                 }
-                if (p.lse) p.lse[row] = kLn2 * (m_used + log2f(l));
+            }
+            if (valid) {
+                if (p.split) {
+                    p.ws_ml[slot * 2] = m_used;
+                    p.ws_ml[slot * 2 + 1] = l;
+                } else if (p.lse) {
+                    p.lse[row] = kLn2 * (m_used + log2f(l));
+                }
+            }
+        } else if (valid) {
+            if (p.split) {
+                const int64_t slot = tile_row(p, b, hkv, f) * p.n_chunks + c;
+                p.ws_ml[slot * 2] = p.ws_ml[slot * 2 + 1] = __int_as_float(0x7fc00000);
             } else {
-                nan_rows(p, b, hkv, f0, rows_unit, r);
+                nan_row(p, b, hkv, f);
             }
         }
     }
@@ -546,24 +628,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #undef BAR
 }
 
-}  // namespace
-
-cudaError_t launch_fmha_tc(const TcParams &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                           const CUtensorMap &tmV, cudaStream_t stream) {
+template <int NT>
+cudaError_t launch_instance(const TcParams &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                            const CUtensorMap &tmV, cudaStream_t stream) {
+    using C = Cfg<NT>;
     static int configured[64] = {0};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 64 && !configured[dev]) {
-        err = cudaFuncSetAttribute(fmha_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kTcSmem);
+        err = cudaFuncSetAttribute(fmha_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   C::kSmem);
         if (err != cudaSuccess) return err;
         configured[dev] = 1;
     }
     const int tiles = p.B * p.Hkv * p.tiles_per_unit;
-    dim3 grid = p.split ? dim3(p.n_chunks, tiles, 1) : dim3(tiles, 1, 1);
-    fmha_tc_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(tmQ, tmK, tmV, p);
+    dim3 grid = p.split ? dim3(p.n_chunks, tiles, 1) : dim3(tiles / NT, 1, 1);
+    fmha_tc_kernel<NT><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fmha_tc(const TcParams &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                           const CUtensorMap &tmV, cudaStream_t stream) {
+    // Two tiles per CTA when two q heads of a group can share every K/V block:
+    // direct output, an even group, prompt rows in whole tiles.
+    const bool pair = !p.split && p.tiles_per_head > 0 && p.G % 2 == 0;
+    return pair ? launch_instance<2>(p, tmQ, tmK, tmV, stream)
+                : launch_instance<1>(p, tmQ, tmK, tmV, stream);
 }
 
 }  // namespace atlas
