@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <limits.h>
+#include <math.h>
 #include <stdint.h>
 #include <mutex>
 
@@ -43,8 +44,12 @@ constexpr int64_t kPlanCtas = 152 * 2 * 8;
 // the output directly once a call has at least this many query tiles.
 constexpr int64_t kTcPlanCtas = 152 * 8;
 constexpr int64_t kTcDirectTiles = 152 * 2;
-// Query tiles whose rows see fewer keys than this use a hi + lo split of P.
+// Query tiles whose rows see fewer keys than this use a hi + lo split of P:
+// with few keys (or a peaked softmax) a single bf16 rounding of P moves the
+// output by up to 2^-9 |v|.  Scores sharper than unit-variance inputs at scale
+// 1/sqrt(D) (|scale| sqrt(D) above kHiLoScale) use the split on every tile.
 constexpr int kHiLoBelow = 512;
+constexpr float kHiLoScale = 1.25f;
 
 enum class Path { SplitBF16, SplitF32, TensorCore };
 
@@ -253,8 +258,9 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         tp.chunk = plan.chunk;
         tp.n_chunks = plan.n_chunks;
         tp.require_full = kind == ATLAS_KIND_PREFILL;
-        tp.hilo_below = kHiLoBelow;
-        tp.scale_log2 = scale * kLog2e;
+        tp.hilo_below = fabsf(scale) * sqrtf((float)D) > kHiLoScale ? INT32_MAX : kHiLoBelow;
+        tp.negate_scores = scale < 0.f;
+        tp.scale_log2 = fabsf(scale) * kLog2e;
         tp.out = L->out;
         tp.out_bf16 = L->out_dtype == ATLAS_BF16;
         tp.lse = L->lse;

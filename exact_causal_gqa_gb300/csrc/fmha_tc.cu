@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(128, 128, false);
+            const uint32_t idS = idesc_bf16_f32(128, 128, false, p.negate_scores != 0);
             constexpr uint32_t idPV = idesc_bf16_f32(128, 128, true);
             bool ok = mbar_wait_bounded(BAR(C::B_Q), 0, abort_flag, kWaitLimitNs);
             tc_fence_after();
@@ -453,30 +453,46 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const uint32_t ts = tl + C::s_col(x, bsel);
             const int nvis = lim_row - (kv_begin + j * BN);  // visible columns of this row
             const bool all_visible = __all_sync(0xffffffffu, nvis >= BN);
-            // Pass 1: row max of the scores (log2 units), eight independent chains.
-            // Outer loops stay rolled: the fully unrolled body overflows the
+            // Pass 1: row max of the raw scores (scale_log2 >= 0, so the scaled
+            // maximum is the maximum scaled), four chains of 3-input max.
+            // Outer loops stay rolled: a fully unrolled body overflows the
             // instruction cache shared with the producer and MMA warps.
-            float mx8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (all_visible) {
 #pragma unroll 1
-            for (int cc = 0; cc < 4; cc += 2) {
-                uint32_t sr[2][32];
-                tmem_ld32(ts + cc * 32, sr[0]);
-                tmem_ld32(ts + cc * 32 + 32, sr[1]);
-                tmem_wait_ld();
+                for (int cc = 0; cc < 4; cc += 2) {
+                    uint32_t sr[2][32];
+                    tmem_ld32(ts + cc * 32, sr[0]);
+                    tmem_ld32(ts + cc * 32 + 32, sr[1]);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
+                    for (int q = 0; q < 2; ++q)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float v = (all_visible || (cc + q) * 32 + e < nvis)
-                                            ? __uint_as_float(sr[q][e]) * p.scale_log2
-                                            : -INFINITY;
-                        mx8[e & 7] = fmaxf(mx8[e & 7], v);
-                    }
+                        for (int e = 0; e < 32; e += 2)
+                            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(sr[q][e]),
+                                                     __uint_as_float(sr[q][e + 1]));
+                }
+            } else {
+#pragma unroll 1
+                for (int cc = 0; cc < 4; cc += 2) {
+                    uint32_t sr[2][32];
+                    tmem_ld32(ts + cc * 32, sr[0]);
+                    tmem_ld32(ts + cc * 32 + 32, sr[1]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int col = (cc + q) * 32 + e;
+                            const float v0 = col < nvis ? __uint_as_float(sr[q][e]) : -INFINITY;
+                            const float v1 =
+                                col + 1 < nvis ? __uint_as_float(sr[q][e + 1]) : -INFINITY;
+                            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], v0, v1);
+                        }
+                }
             }
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float mraw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;
             float corr = 1.f;
             if (mx > m_used + kRescaleThreshold) {
                 corr = ex2(m_used - mx);  // 0 on the first visible block
@@ -507,10 +523,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             // written over columns of S already read -- keys 64h .. 64h+63 go to
             // columns 64h .. 64h+31 (keys 2k, 2k+1 in one column) and, when
             // requested, their remainders P - bf16(P) to columns 64h+32 .. 64h+63.
-            float rs8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
             if (r == 0) TRACE(2 + x, 5, j);
+            float2 rs2[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) rs2[k] = make_float2(0.f, 0.f);
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm2 = make_float2(-mref, -mref);
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 uint32_t sr[2][32];
@@ -522,26 +540,30 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     uint32_t hw[16], lw[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
-                        const int c0 = h * 64 + q * 32 + 2 * k;
-                        const float s0 = __uint_as_float(sr[q][2 * k]) * p.scale_log2;
-                        const float s1 = __uint_as_float(sr[q][2 * k + 1]) * p.scale_log2;
-                        const float a = (all_visible || c0 < nvis) ? ex2(s0 - mref) : 0.f;
-                        const float bb = (all_visible || c0 + 1 < nvis) ? ex2(s1 - mref) : 0.f;
-                        rs8[(2 * k) & 7] += a;
-                        rs8[(2 * k + 1) & 7] += bb;
-                        const __nv_bfloat162 hv = __floats2bfloat162_rn(a, bb);
+                        // 2^(s * scale_log2 - m) for keys 2k, 2k+1 of this quarter
+                        float2 t = ffma2(make_float2(__uint_as_float(sr[q][2 * k]),
+                                                     __uint_as_float(sr[q][2 * k + 1])),
+                                         sc2, nm2);
+                        if (!all_visible) {
+                            const int c0 = h * 64 + q * 32 + 2 * k;
+                            t.x = c0 < nvis ? t.x : -INFINITY;
+                            t.y = c0 + 1 < nvis ? t.y : -INFINITY;
+                        }
+                        const float2 e2 = make_float2(ex2(t.x), ex2(t.y));
+                        rs2[k & 3] = fadd2(rs2[k & 3], e2);
+                        const __nv_bfloat162 hv = __floats2bfloat162_rn(e2.x, e2.y);
                         hw[k] = *reinterpret_cast<const uint32_t *>(&hv);
                         if (hilo) {
                             const float2 hf = __bfloat1622float2(hv);
-                            lw[k] = pack_bf16(a - hf.x, bb - hf.y);
+                            lw[k] = pack_bf16(e2.x - hf.x, e2.y - hf.y);
                         }
                     }
                     tmem_st16(ts + h * 64 + q * 16, hw);
                     if (hilo) tmem_st16(ts + h * 64 + 32 + q * 16, lw);
                 }
             }
-            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
-                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
+            const float rs = (r01.x + r01.y) + (r23.x + r23.y);
             l = l * corr + rs;
             if (r == 0) TRACE(2 + x, 6, j + 0 * (int)(l != l));
             tmem_wait_st();

@@ -63,7 +63,8 @@ struct TcParams {
     int32_t chunk, n_chunks;  // split geometry (chunk a multiple of 128)
     int32_t require_full;
     int32_t hilo_below;       // tiles whose rows see fewer keys use a hi+lo split of P
-    float scale_log2;
+    int32_t negate_scores;    // scale < 0: S = -Q K^T with |scale| (keeps the max exact)
+    float scale_log2;         // |scale| * log2(e)
     void *out;
     int32_t out_bf16;
     float *lse;

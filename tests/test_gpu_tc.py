@@ -145,3 +145,17 @@ def test_config5_prefill_full_size_sampled_rows():
              for i in (0, 1, 2, 63, 127, 128, 511, 512, 4095, S - 1)]
     rows = np.unique(np.concatenate([rng.choice(flat_rows(prob), 64, replace=False), early]))
     sampled(prob, rows, out32, out16)
+
+
+@pytest.mark.parametrize("scale", [-0.07, 0.0, 0.31])
+def test_tc_any_finite_scale(scale):
+    # S = -Q K^T with |scale| for negative scales; scale 0 gives uniform weights.
+    prob = inputs.make("suffix", 2, 32, 4, 128, 32, [200, 1000], q_len=16, seed=7, scale=scale)
+    check(prob)
+    prob = inputs.make("prefill", 1, 8, 2, 128, 64, [384], seed=8, scale=scale)
+    check(prob, flags=atlas.DEBUG_TC_DIRECT)
+
+
+def test_decode_any_finite_scale():
+    prob = inputs.make("decode", 3, 16, 4, 128, 16, [5, 300, 2000], seed=9, scale=-0.2)
+    check(prob)
