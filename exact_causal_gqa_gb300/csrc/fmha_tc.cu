@@ -460,35 +460,28 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (all_visible) {
 #pragma unroll 1
-                for (int cc = 0; cc < 4; cc += 2) {
-                    uint32_t sr[2][32];
-                    tmem_ld32(ts + cc * 32, sr[0]);
-                    tmem_ld32(ts + cc * 32 + 32, sr[1]);
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32];
+                    tmem_ld32(ts + cc * 32, sr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 2; ++q)
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2)
-                            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(sr[q][e]),
-                                                     __uint_as_float(sr[q][e + 1]));
+                    for (int e = 0; e < 32; e += 2)
+                        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(sr[e]),
+                                                 __uint_as_float(sr[e + 1]));
                 }
             } else {
 #pragma unroll 1
-                for (int cc = 0; cc < 4; cc += 2) {
-                    uint32_t sr[2][32];
-                    tmem_ld32(ts + cc * 32, sr[0]);
-                    tmem_ld32(ts + cc * 32 + 32, sr[1]);
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32];
+                    tmem_ld32(ts + cc * 32, sr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 2; ++q)
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const int col = (cc + q) * 32 + e;
-                            const float v0 = col < nvis ? __uint_as_float(sr[q][e]) : -INFINITY;
-                            const float v1 =
-                                col + 1 < nvis ? __uint_as_float(sr[q][e + 1]) : -INFINITY;
-                            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], v0, v1);
-                        }
+                    for (int e = 0; e < 32; e += 2) {
+                        const int col = cc * 32 + e;
+                        const float v0 = col < nvis ? __uint_as_float(sr[e]) : -INFINITY;
+                        const float v1 = col + 1 < nvis ? __uint_as_float(sr[e + 1]) : -INFINITY;
+                        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], v0, v1);
+                    }
                 }
             }
             const float mraw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
@@ -529,37 +522,54 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             for (int k = 0; k < 4; ++k) rs2[k] = make_float2(0.f, 0.f);
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-mref, -mref);
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sr[2][32];
-                tmem_ld32(ts + h * 64, sr[0]);
-                tmem_ld32(ts + h * 64 + 32, sr[1]);
-                tmem_wait_ld();
+            // Keys 2k, 2k+1 of quarter cc (columns 32cc..32cc+31 of S) -> P pair k,
+            // written to column 64*(cc/2) + 16*(cc%2) + k: always a column of S that
+            // has been read already.  The remainder goes 32 columns further on, so
+            // with the split the two quarters of a half are read before writing.
+            auto quarter = [&](const uint32_t (&sr)[32], int cc, uint32_t (&hw)[16],
+                               uint32_t (&lw)[16], bool masked, bool split) {
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t hw[16], lw[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        // 2^(s * scale_log2 - m) for keys 2k, 2k+1 of this quarter
-                        float2 t = ffma2(make_float2(__uint_as_float(sr[q][2 * k]),
-                                                     __uint_as_float(sr[q][2 * k + 1])),
-                                         sc2, nm2);
-                        if (!all_visible) {
-                            const int c0 = h * 64 + q * 32 + 2 * k;
-                            t.x = c0 < nvis ? t.x : -INFINITY;
-                            t.y = c0 + 1 < nvis ? t.y : -INFINITY;
-                        }
-                        const float2 e2 = make_float2(ex2(t.x), ex2(t.y));
-                        rs2[k & 3] = fadd2(rs2[k & 3], e2);
-                        const __nv_bfloat162 hv = __floats2bfloat162_rn(e2.x, e2.y);
-                        hw[k] = *reinterpret_cast<const uint32_t *>(&hv);
-                        if (hilo) {
-                            const float2 hf = __bfloat1622float2(hv);
-                            lw[k] = pack_bf16(e2.x - hf.x, e2.y - hf.y);
-                        }
+                for (int k = 0; k < 16; ++k) {
+                    float2 t = ffma2(make_float2(__uint_as_float(sr[2 * k]),
+                                                 __uint_as_float(sr[2 * k + 1])),
+                                     sc2, nm2);
+                    if (masked) {
+                        const int c0 = cc * 32 + 2 * k;
+                        t.x = c0 < nvis ? t.x : -INFINITY;
+                        t.y = c0 + 1 < nvis ? t.y : -INFINITY;
                     }
-                    tmem_st16(ts + h * 64 + q * 16, hw);
-                    if (hilo) tmem_st16(ts + h * 64 + 32 + q * 16, lw);
+                    const float2 e2 = make_float2(ex2(t.x), ex2(t.y));
+                    rs2[k & 3] = fadd2(rs2[k & 3], e2);
+                    const __nv_bfloat162 hv = __floats2bfloat162_rn(e2.x, e2.y);
+                    hw[k] = *reinterpret_cast<const uint32_t *>(&hv);
+                    if (split) {
+                        const float2 hf = __bfloat1622float2(hv);
+                        lw[k] = pack_bf16(e2.x - hf.x, e2.y - hf.y);
+                    }
+                }
+            };
+            if (!hilo && all_visible) {
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32], hw[16], lw[16];
+                    tmem_ld32(ts + cc * 32, sr);
+                    tmem_wait_ld();
+                    quarter(sr, cc, hw, lw, false, false);
+                    tmem_st16(ts + (cc >> 1) * 64 + (cc & 1) * 16, hw);
+                }
+            } else {
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t sr0[32], sr1[32], hw[16], lw[16];
+                    tmem_ld32(ts + h * 64, sr0);
+                    tmem_ld32(ts + h * 64 + 32, sr1);
+                    tmem_wait_ld();
+                    quarter(sr0, 2 * h, hw, lw, !all_visible, hilo);
+                    tmem_st16(ts + h * 64, hw);
+                    if (hilo) tmem_st16(ts + h * 64 + 32, lw);
+                    quarter(sr1, 2 * h + 1, hw, lw, !all_visible, hilo);
+                    tmem_st16(ts + h * 64 + 16, hw);
+                    if (hilo) tmem_st16(ts + h * 64 + 48, lw);
                 }
             }
             const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
