@@ -84,14 +84,22 @@ KERNEL_SOURCES = {"split_bf16_kernel": "split_kv.cu", "split_f32_kernel": "split
                   "fmha_tc_kernel": "fmha_tc.cu"}
 
 
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the kernel's translation unit and the headers it shares."""
+    csrc = os.path.join(ROOT, "exact_causal_gqa_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (KERNEL_SOURCES[kernel], "ptx.cuh", "internal.h"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
     kernel source is unchanged since it was captured; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = os.path.join(ROOT, "exact_causal_gqa_gb300", "csrc", KERNEL_SOURCES[kernel])
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha(kernel)
     for line in open(path):
         parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if parts.get("kernel") == kernel and parts.get("workload") == workload and \
