@@ -53,6 +53,24 @@ def parse_args():
     return ap.parse_args()
 
 
+def rank_seed(config_index: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling: per-rank work is fixed)."""
+    return config_index + 1000 * rank
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The slowest rank's time (identity when torch.distributed is not initialised)."""
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_max: float, scale: float) -> float:
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return world * units_per_rank / (ms_max * 1e-3) / scale
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -176,7 +194,7 @@ def run_atlas(args, world, rank, local):
     torch.cuda.set_device(dev)
     atlas.load_library()
     cfg = inputs.CONFIGS[args.config]
-    seed = args.config + 1000 * rank
+    seed = rank_seed(args.config, rank)
     overrides = {"B": args.batch} if args.batch else {}
     prob = inputs.make_config(args.config, seed=seed, device=dev, **overrides)
     kv_bytes, flops = work_of(prob)
@@ -232,10 +250,7 @@ def run_atlas(args, world, rank, local):
     step_ms = [s.elapsed_time(e) for s, e in zip(step_start, step_end)]
     main_ms = [t.main_ms() for t in timers]
     ms = sum(step_ms) / len(step_ms)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, dev)
     status_val = int(status.item())
 
     # ---- end to end: pinned host inputs -> device -> kernels -> host output
@@ -267,10 +282,7 @@ def run_atlas(args, world, rank, local):
             e2e_step()
         ev1.record()
         torch.cuda.synchronize(dev)
-        e_ms = torch.tensor([ev0.elapsed_time(ev1) / e_steps], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(e_ms, op=torch.distributed.ReduceOp.MAX)
-        e2e = (float(e_ms.item()), bi, bo)
+        e2e = (max_over_ranks(ev0.elapsed_time(ev1) / e_steps, dev), bi, bo)
 
     if rank != 0:
         return None
@@ -278,13 +290,13 @@ def run_atlas(args, world, rank, local):
     decode_like = prob.kind != "prefill"
     main_avg = sum(main_ms) / len(main_ms)
     if decode_like:
-        value = world * kv_bytes / (ms_max * 1e-3) / 1e9
+        value = job_rate(kv_bytes, world, ms_max, 1e9)
         unit = "GB/s"
         achieved = kv_bytes / (main_avg * 1e-3) / 1e9
         peak = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
         bound = "hbm"
     else:
-        value = world * flops / (ms_max * 1e-3) / 1e12
+        value = job_rate(flops, world, ms_max, 1e12)
         unit = "TFLOP/s"
         achieved = flops / (main_avg * 1e-3) / 1e12
         peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
@@ -351,8 +363,8 @@ def run_atlas(args, world, rank, local):
     line["clocks"] = clk
     if e2e is not None:
         e_ms, bi, bo = e2e
-        e_val = (world * kv_bytes / (e_ms * 1e-3) / 1e9) if decode_like else \
-            (world * flops / (e_ms * 1e-3) / 1e12)
+        e_val = job_rate(kv_bytes, world, e_ms, 1e9) if decode_like else \
+            job_rate(flops, world, e_ms, 1e12)
         line["e2e"] = {"value": round(e_val, 3), "unit": unit, "ms_per_step": round(e_ms, 4),
                        "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
     if not args.no_cpu_baseline:
