@@ -36,9 +36,12 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // CTAs the automatic split plan aims for at the largest context the page table
-// allows: 152 SMs x 2 resident CTAs x 8 waves.  A pure function of the call's
-// sizes, so a given problem always gets the same split (and the same bits).
-constexpr int64_t kPlanCtas = 152 * 2 * 8;
+// allows: 152 SMs x 2 resident CTAs x 2 waves, with splits of at most
+// kMaxSplit keys (measured best at 2.5K-4K keys, ~1.3-2 MB of K/V per CTA, on the
+// decode workloads).  A pure function of the call's sizes, so a given problem
+// always gets the same split (and the same bits).
+constexpr int64_t kPlanCtas = 152 * 2 * 2;
+constexpr int64_t kMaxSplit = 2560;
 
 // The tensor-core path's split plan aims for 152 SMs x 1 CTA x 8 waves; it writes
 // the output directly once a call has at least this many query tiles.
@@ -135,8 +138,10 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     if (chunk == 0) {
         const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
         chunk = round_up((max_ctx * units + kPlanCtas - 1) / kPlanCtas, kSplitBlockTokens);
-        if (chunk < 512) chunk = 512;
-        if (chunk > 8192) chunk = 8192;
+        // The f32 kernel has no pipeline to fill: small splits just add CTAs.
+        const int64_t min_chunk = plan->path == Path::SplitF32 ? kSplitBlockTokens : 512;
+        if (chunk > kMaxSplit) chunk = kMaxSplit;
+        if (chunk < min_chunk) chunk = min_chunk;
     }
     if (chunk > max_ctx) chunk = round_up(max_ctx, kSplitBlockTokens);
     plan->chunk = (int)chunk;

@@ -257,6 +257,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
 
     if (warp == 0) {
         // -------------------------------------------------------- TMA producer
+        // The whole warp walks the blocks (page ids come from a warp-wide cache);
+        // lane 0 issues the copies.
         if (lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
@@ -267,46 +269,52 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 tma_load_2d(sb + C::OFF_Q + x * kTileBytes, &tmQ, 0, qrow, BAR(C::B_Q));
                 tma_load_2d(sb + C::OFF_Q + x * kTileBytes + kSlab, &tmQ, 64, qrow, BAR(C::B_Q));
             }
-            const int BR = p.P < BN ? p.P : BN;
-            int issued_k = 0, issued_v = 0;
-            for (int j = 0; j < nb && !failed; ++j) {
-                const int s = j % S, use = j / S;
-                const int kb = kv_begin + j * BN;
-                const int ke = min(kb + BN, kv_end);
-                const int nbox = (ke - kb + BR - 1) / BR;
-                const uint32_t bytes = (uint32_t)(nbox * BR * 128 * 2);
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int full = (kv == 0 ? C::B_KFULL : C::B_VFULL) + s;
-                    const int empty = (kv == 0 ? C::B_KEMPTY : C::B_VEMPTY) + s;
-                    if (use > 0 &&
-                        !mbar_wait_bounded(BAR(empty), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
-                        failed = true;
-                        break;
-                    }
+        }
+        PageIdCache pages{p.page_table + (int64_t)b * p.max_pages, (kv_end - 1) / p.P};
+        const int BR = p.P < BN ? p.P : BN;
+        int issued_k = 0, issued_v = 0;
+        for (int j = 0; j < nb && !failed; ++j) {
+            const int s = j % S, use = j / S;
+            const int kb = kv_begin + j * BN;
+            const int ke = min(kb + BN, kv_end);
+            const int nbox = (ke - kb + BR - 1) / BR;
+            const uint32_t bytes = (uint32_t)(nbox * BR * 128 * 2);
+            // y coordinate of box bx of this block (lane bx holds it; nbox <= 16)
+            int my_y = 0;
+            for (int bx = 0; bx < nbox; ++bx) {
+                const int tk = kb + bx * BR;
+                const int y = (pages.get(tk / p.P) * p.Hkv + hkv) * p.P + (tk % p.P);
+                if (lane == bx) my_y = y;
+            }
+            for (int kv = 0; kv < 2; ++kv) {
+                const int full = (kv == 0 ? C::B_KFULL : C::B_VFULL) + s;
+                const int empty = (kv == 0 ? C::B_KEMPTY : C::B_VEMPTY) + s;
+                if (use > 0 && !wait_warp(BAR(empty), (use - 1) & 1, abort_flag)) {
+                    failed = true;
+                    break;
+                }
+                if (lane < nbox) {
                     const CUtensorMap *map = kv == 0 ? &tmK : &tmV;
                     const uint32_t dst = sb + (kv == 0 ? C::OFF_K : C::OFF_V) + s * kTileBytes;
-                    mbar_arrive_expect_tx(BAR(full), bytes);
-                    for (int bx = 0; bx < nbox; ++bx) {
-                        const int tk = kb + bx * BR;
-                        const int phys = p.page_table[(int64_t)b * p.max_pages + tk / p.P];
-                        const int y = (phys * p.Hkv + hkv) * p.P + (tk % p.P);
-                        tma_load_2d(dst + bx * BR * 128, map, 0, y, BAR(full));
-                        tma_load_2d(dst + kSlab + bx * BR * 128, map, 64, y, BAR(full));
-                    }
-                    if (kv == 0) issued_k = j + 1;
-                    else issued_v = j + 1;
-                    TRACE(0, kv, j);
+                    if (lane == 0) mbar_arrive_expect_tx(BAR(full), bytes);
+                    __syncwarp((1u << nbox) - 1u);
+                    tma_load_2d(dst + lane * BR * 128, map, 0, my_y, BAR(full));
+                    tma_load_2d(dst + kSlab + lane * BR * 128, map, 64, my_y, BAR(full));
                 }
+                __syncwarp();
+                if (kv == 0) issued_k = j + 1;
+                else issued_v = j + 1;
+                TRACE(0, kv, j);
             }
-            if (failed) {
-                *abort_flag = 1;
-                int no_abort = 0;
-                mbar_wait_bounded(BAR(C::B_Q), 0, &no_abort, kWaitLimitNs);
-                for (int j = max(0, issued_k - S); j < issued_k; ++j)
-                    mbar_wait_bounded(BAR(C::B_KFULL + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
-                for (int j = max(0, issued_v - S); j < issued_v; ++j)
-                    mbar_wait_bounded(BAR(C::B_VFULL + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
-            }
+        }
+        if (failed && lane == 0) {
+            *abort_flag = 1;
+            int no_abort = 0;
+            mbar_wait_bounded(BAR(C::B_Q), 0, &no_abort, kWaitLimitNs);
+            for (int j = max(0, issued_k - S); j < issued_k; ++j)
+                mbar_wait_bounded(BAR(C::B_KFULL + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
+            for (int j = max(0, issued_v - S); j < issued_v; ++j)
+                mbar_wait_bounded(BAR(C::B_VFULL + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -494,28 +502,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const float mref = m_used == -INFINITY ? 0.f : m_used;
             if (r == 0) TRACE(2 + x, 3, j + 0 * (int)(mref != mref));
 
-            // O must hold PV(j-1) before it is rescaled.  With one S buffer the
-            // MMA issued S(j) only after PV(j-1) completed, so S being full says so.
-            if (SB > 1 && j > 0 && !wait_warp(BAR(C::B_PVDONE + x), (j - 1) & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(to + cc * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-                    tmem_st32(to + cc * 32, o);
-                }
-            }
-            // Pass 2, one half (64 keys) at a time: P = 2^(s - m) as bf16 pairs
-            // written over columns of S already read -- keys 64h .. 64h+63 go to
-            // columns 64h .. 64h+31 (keys 2k, 2k+1 in one column) and, when
-            // requested, their remainders P - bf16(P) to columns 64h+32 .. 64h+63.
+            // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs, written over columns
+            // of S already read (see quarter() below), and the row sum.
             if (r == 0) TRACE(2 + x, 5, j);
             float2 rs2[4];
 #pragma unroll
@@ -576,6 +564,26 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const float rs = (r01.x + r01.y) + (r23.x + r23.y);
             l = l * corr + rs;
             if (r == 0) TRACE(2 + x, 6, j + 0 * (int)(l != l));
+            // O must hold PV(j-1) before it is rescaled (and before PV(j) is issued,
+            // which waits for this warpgroup's P).  Doing it after writing P keeps
+            // PV(j-1) off the critical path.  With one S buffer the MMA issued S(j)
+            // only after PV(j-1) completed, so S being full already says so.
+            if (SB > 1 && j > 0 && !wait_warp(BAR(C::B_PVDONE + x), (j - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(to + cc * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+                    tmem_st32(to + cc * 32, o);
+                }
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(C::B_PFULL + x));

@@ -128,6 +128,26 @@ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// Page ids of one sequence, read by a whole warp 32 at a time and handed out by
+// shuffle: the producer pays one coalesced table load per 32 pages instead of a
+// dependent global load before every TMA box.  All 32 lanes call get() with the
+// same (warp-uniform) logical page index.
+struct PageIdCache {
+    const int32_t *row;  // page_table + b * max_pages
+    int last;            // highest logical page that may be read
+    int base = -64;
+    int mine = 0;
+    __device__ __forceinline__ int get(int pg) {
+        const int lane = threadIdx.x & 31;
+        const int nb = pg & ~31;
+        if (nb != base) {
+            base = nb;
+            mine = (nb + lane <= last) ? row[nb + lane] : 0;
+        }
+        return __shfl_sync(0xffffffffu, mine, pg - nb);
+    }
+};
+
 // ---------------------------------------------------------------- mma.sync path
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
                                             uint32_t &r2, uint32_t &r3) {

@@ -181,50 +181,59 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer warp
+        // The whole warp walks the blocks (page ids from a warp-wide cache, one
+        // coalesced table read per 32 pages); lanes 0..subs-1 issue the boxes.
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            const uint64_t policy = policy_evict_first();
-            const int BR = p.P < BT ? p.P : BT;  // rows per box
-            const int subs = BT / BR;
-            int issued = 0;
-            for (int j = 0; j < nblocks; ++j) {
-                const int s = j % STAGES;
-                if (j >= STAGES &&
-                    !mbar_wait_bounded(empty0 + 8 * s, ((j / STAGES) - 1) & 1, abort_flag,
-                                       kWaitLimitNs)) {
-                    failed = true;
-                    break;
-                }
-                const int t0 = kv_begin + j * BT;
-                const int nsub = min(subs, (kv_end - t0 + BR - 1) / BR);
-                if ((p.debug_flags & ATLAS_DEBUG_WITHHOLD_STAGE) && j == 0) continue;
-                mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nsub * BR * D * 2 * 2));
+        }
+        const uint64_t policy = policy_evict_first();
+        const int BR = p.P < BT ? p.P : BT;  // rows per box
+        const int subs = BT / BR;           // boxes per block (<= 8)
+        PageIdCache pages{p.page_table + (int64_t)b * p.max_pages, (kv_end - 1) / p.P};
+        int issued = 0;
+        for (int j = 0; j < nblocks; ++j) {
+            const int s = j % STAGES;
+            if (j >= STAGES &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * s, ((j / STAGES) - 1) & 1,
+                                                           abort_flag, kWaitLimitNs))) {
+                failed = true;
+                break;
+            }
+            const int t0 = kv_begin + j * BT;
+            const int nsub = min(subs, (kv_end - t0 + BR - 1) / BR);
+            int my_y = 0;
+            for (int sb = 0; sb < nsub; ++sb) {
+                const int t = t0 + sb * BR;
+                const int y = (pages.get(t / p.P) * p.Hkv + hkv) * p.P + (t % p.P);
+                if (lane == sb) my_y = y;
+            }
+            if ((p.debug_flags & ATLAS_DEBUG_WITHHOLD_STAGE) && j == 0) continue;
+            if (lane < nsub) {
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nsub * BR * D * 2 * 2));
+                __syncwarp((1u << nsub) - 1u);
                 const uint32_t kdst = sbase + s * Lay::kStage;
                 const uint32_t vdst = kdst + Lay::kTile;
-                for (int sb = 0; sb < nsub; ++sb) {
-                    const int t = t0 + sb * BR;
-                    const int phys = p.page_table[(int64_t)b * p.max_pages + t / p.P];
-                    const int y = (phys * p.Hkv + hkv) * p.P + (t % p.P);
 #pragma unroll
-                    for (int slab = 0; slab < D / 64; ++slab) {
-                        tma_load_2d_hint(kdst + slab * SLAB + sb * BR * 128, &tmK, slab * 64, y,
-                                         full0 + 8 * s, policy);
-                        tma_load_2d_hint(vdst + slab * SLAB + sb * BR * 128, &tmV, slab * 64, y,
-                                         full0 + 8 * s, policy);
-                    }
+                for (int slab = 0; slab < D / 64; ++slab) {
+                    tma_load_2d_hint(kdst + slab * SLAB + lane * BR * 128, &tmK, slab * 64, my_y,
+                                     full0 + 8 * s, policy);
+                    tma_load_2d_hint(vdst + slab * SLAB + lane * BR * 128, &tmV, slab * 64, my_y,
+                                     full0 + 8 * s, policy);
                 }
-                issued = j + 1;
             }
-            if (failed) {
-                *abort_flag = 1;
-                // Let the copies already in flight land before the CTA exits.
-                int no_abort = 0;
-                for (int j = max(0, issued - STAGES); j < issued; ++j) {
-                    if ((p.debug_flags & ATLAS_DEBUG_WITHHOLD_STAGE) && j == 0) continue;
-                    mbar_wait_bounded(full0 + 8 * (j % STAGES), (j / STAGES) & 1,
-                                      (volatile int *)&no_abort, kWaitLimitNs);
-                }
+            __syncwarp();
+            issued = j + 1;
+        }
+        if (failed && lane == 0) {
+            *abort_flag = 1;
+            // Let the copies already in flight land before the CTA exits.
+            int no_abort = 0;
+            for (int j = max(0, issued - STAGES); j < issued; ++j) {
+                if ((p.debug_flags & ATLAS_DEBUG_WITHHOLD_STAGE) && j == 0) continue;
+                mbar_wait_bounded(full0 + 8 * (j % STAGES), (j / STAGES) & 1,
+                                  (volatile int *)&no_abort, kWaitLimitNs);
             }
         }
         __syncwarp();
@@ -446,31 +455,45 @@ __global__ void __launch_bounds__(128)
         m_run[c] = -INFINITY;
         l_run[c] = 0.f;
     }
-    for (int t = kv_begin + warp; t < kv_end; t += W) {
-        const int phys = p.page_table[(int64_t)b * p.max_pages + t / p.P];
-        const int64_t base = (((int64_t)phys * p.Hkv + hkv) * p.P + t % p.P) * D + lane * DPL;
-        float kr[DPL], vr[DPL];
+    // Each warp takes 4 consecutive keys per step (its K/V rows are loaded
+    // together, so their memory latencies overlap) and every 4th such group.
+    constexpr int U = 4;
+    for (int t0 = kv_begin + warp * U; t0 < kv_end; t0 += W * U) {
+        float kr[U][DPL], vr[U][DPL];
 #pragma unroll
-        for (int j = 0; j < DPL; ++j) {
-            kr[j] = kp[base + j];
-            vr[j] = vp[base + j];
+        for (int u = 0; u < U; ++u) {
+            const int t = t0 + u;
+            if (t < kv_end) {
+                const int phys = p.page_table[(int64_t)b * p.max_pages + t / p.P];
+                const int64_t base =
+                    (((int64_t)phys * p.Hkv + hkv) * p.P + t % p.P) * D + lane * DPL;
+#pragma unroll
+                for (int j = 0; j < DPL; ++j) {
+                    kr[u][j] = kp[base + j];
+                    vr[u][j] = vp[base + j];
+                }
+            }
         }
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            if (t >= lim[c]) continue;  // warp-uniform
-            float dot = 0.f;
+        for (int u = 0; u < U; ++u) {
+            const int t = t0 + u;
 #pragma unroll
-            for (int j = 0; j < DPL; ++j) dot = fmaf(qv[c][j], kr[j], dot);
+            for (int c = 0; c < NC; ++c) {
+                if (t >= lim[c]) continue;  // warp-uniform (lim <= kv_end)
+                float dot = 0.f;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            const float s2 = dot * p.scale_log2;
-            const float m_new = fmaxf(m_run[c], s2);
-            const float corr = ex2(m_run[c] - m_new);
-            const float pw = ex2(s2 - m_new);
-            l_run[c] = l_run[c] * corr + pw;
+                for (int j = 0; j < DPL; ++j) dot = fmaf(qv[c][j], kr[u][j], dot);
 #pragma unroll
-            for (int j = 0; j < DPL; ++j) accv[c][j] = fmaf(pw, vr[j], accv[c][j] * corr);
-            m_run[c] = m_new;
+                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                const float s2 = dot * p.scale_log2;
+                const float m_new = fmaxf(m_run[c], s2);
+                const float corr = ex2(m_run[c] - m_new);
+                const float pw = ex2(s2 - m_new);
+                l_run[c] = l_run[c] * corr + pw;
+#pragma unroll
+                for (int j = 0; j < DPL; ++j) accv[c][j] = fmaf(pw, vr[u][j], accv[c][j] * corr);
+                m_run[c] = m_new;
+            }
         }
     }
 #pragma unroll
