@@ -43,9 +43,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr int64_t kPlanCtas = 152 * 2 * 2;
 constexpr int64_t kMaxSplit = 2560;
 
-// The tensor-core path's split plan aims for 152 SMs x 1 CTA x 8 waves; it writes
-// the output directly once a call has at least this many query tiles.
-constexpr int64_t kTcPlanCtas = 152 * 8;
+// The tensor-core path's split plan aims for 152 SMs x 1 CTA x 3 waves at the
+// largest context (splits of 1K-8K keys; 8K measured best for the suffix
+// workload); it writes the output directly once a call has at least
+// kTcDirectTiles query tiles.
+constexpr int64_t kTcPlanCtas = 152 * 3;
 constexpr int64_t kTcDirectTiles = 152 * 2;
 // Query tiles whose rows see fewer keys than this use a hi + lo split of P:
 // with few keys (or a peaked softmax) a single bf16 rounding of P moves the
@@ -109,7 +111,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         } else if (tiles < kTcDirectTiles && !(L->debug_flags & ATLAS_DEBUG_TC_DIRECT)) {
             chunk = round_up((max_ctx * tiles + kTcPlanCtas - 1) / kTcPlanCtas, 128);
             if (chunk < 1024) chunk = 1024;
-            if (chunk > 16384) chunk = 16384;
+            if (chunk > 8192) chunk = 8192;
         }
         if (chunk > 0) {
             if (chunk > round_up(max_ctx, 128)) chunk = round_up(max_ctx, 128);
