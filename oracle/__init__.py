@@ -57,10 +57,10 @@ def _load():
         I = ctypes.c_int
         L = ctypes.c_int64
         Dd = ctypes.c_double
-        common = [P, P, P, P, P, I, I, I, I, I, I, I, I, Dd]
+        common = [P, P, P, P, P, I, I, I, I, I, I, I, I, Dd, I, Dd]
         for name in ("oracle_attn", "oracle_folded"):
             fn = getattr(lib, name)
-            fn.argtypes = common + [P, L, P, P]
+            fn.argtypes = common + [P, P, L, P, P]
             fn.restype = I
         lib.oracle_state.argtypes = common + [L, L, L, P, P, P]
         lib.oracle_state.restype = I
@@ -118,11 +118,14 @@ def _prepare(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads):
 
 
 def _run(name, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scale,
-         rows=None, want_lse=False):
+         rows=None, want_lse=False, window=0, softcap=0.0, sinks=None):
     lib = _load()
     q, k, v, table, lens, dims = _prepare(q, k_pages, v_pages, page_table, seq_lens,
                                           n_q_heads, n_kv_heads)
     B, Hq, Hkv, D, P, max_pages, num_pages, q_len = dims
+    sinks_arr = None if sinks is None else _f32(sinks)
+    if sinks_arr is not None and sinks_arr.shape != (Hq,):
+        raise OracleError("sinks must hold one logit per q head")
     if rows is None:
         n_rows = B * Hq * q_len
         rows_arr = None
@@ -133,6 +136,7 @@ def _run(name, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads,
     lse = np.empty(n_rows, dtype=np.float64) if want_lse else None
     rc = getattr(lib, name)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(table), _ptr(lens), *dims, float(scale),
+        int(window), float(softcap), _ptr(sinks_arr) if sinks_arr is not None else None,
         _ptr(rows_arr) if rows_arr is not None else None, n_rows,
         _ptr(out), _ptr(lse) if lse is not None else None)
     if rc:
@@ -145,27 +149,29 @@ def _run(name, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads,
 
 
 def attn(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scale,
-         rows=None, want_lse=False):
+         rows=None, want_lse=False, window=0, softcap=0.0, sinks=None):
     """Full-KV causal GQA attention in fp64.
 
     q[B][Hq][q_len][D]; pools [num_pages][Hkv][P][D]; page_table[B][max_pages];
     seq_lens[B].  Query row i of sequence b sits at position seq_lens[b] - q_len + i
-    and sees keys 0..that position.  ``rows`` (flat indices (b*Hq+h)*q_len+i)
-    restricts the output to those rows, returned as [len(rows)][D].
+    and sees keys 0..that position (only the last ``window`` of them when window > 0);
+    ``softcap`` c > 0 maps each scaled score s to c tanh(s / c); ``sinks`` (one logit
+    per q head) adds exp(sink) to the softmax denominator.  ``rows`` (flat indices
+    (b*Hq+h)*q_len+i) restricts the output to those rows, returned as [len(rows)][D].
     """
     return _run("oracle_attn", q, k_pages, v_pages, page_table, seq_lens, n_q_heads,
-                n_kv_heads, scale, rows, want_lse)
+                n_kv_heads, scale, rows, want_lse, window, softcap, sinks)
 
 
 def folded(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scale,
-           rows=None, want_lse=False):
+           rows=None, want_lse=False, window=0, softcap=0.0, sinks=None):
     """The same result reached by folding one page at a time into (m, l, acc)."""
     return _run("oracle_folded", q, k_pages, v_pages, page_table, seq_lens, n_q_heads,
-                n_kv_heads, scale, rows, want_lse)
+                n_kv_heads, scale, rows, want_lse, window, softcap, sinks)
 
 
 def state(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scale,
-          row, t_begin, t_end):
+          row, t_begin, t_end, window=0, softcap=0.0):
     """(m, l, acc) of flat row ``row`` over its visible keys in [t_begin, t_end)."""
     lib = _load()
     q, k, v, table, lens, dims = _prepare(q, k_pages, v_pages, page_table, seq_lens,
@@ -175,8 +181,8 @@ def state(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scal
     l = np.zeros(1)
     acc = np.zeros(D)
     rc = lib.oracle_state(_ptr(q), _ptr(k), _ptr(v), _ptr(table), _ptr(lens), *dims,
-                          float(scale), int(row), int(t_begin), int(t_end),
-                          _ptr(m), _ptr(l), _ptr(acc))
+                          float(scale), int(window), float(softcap), int(row), int(t_begin),
+                          int(t_end), _ptr(m), _ptr(l), _ptr(acc))
     if rc:
         raise OracleError(f"oracle_state: {_ERRORS.get(rc, rc)}")
     return float(m[0]), float(l[0]), acc

@@ -31,6 +31,14 @@
  *  - ferrox-core crate index, "attention" module: the vanilla causal GQA path
  *    is the correctness baseline.
  *
+ * Score and mask variants (ferrox-core crate index: causal_gqa_attention_windowed,
+ * _softcap and _sinks; readings of their names, since the index gives no formula):
+ *   window W > 0   row i sees only keys pos - W < t <= pos (the W most recent);
+ *   softcap c > 0  s_t = c * tanh(scale * <q, k_t> / c);
+ *   sinks          one extra logit sink[h] per q head joins the denominator with no
+ *                  value row: l += exp(sink[h] - M), M = max(M, sink[h]).
+ * W = 0, c = 0 and sinks == NULL give plain attention.
+ *
  * All inputs are fp32 arrays holding the exact stored values (bf16 inputs are
  * widened exactly by the caller); all arithmetic is fp64.
  *
@@ -51,6 +59,9 @@ typedef struct {
     const int32_t *table, *lens;
     int B, Hq, Hkv, D, P, max_pages, num_pages, q_len;
     double scale;
+    int window;          /* 0: none */
+    double softcap;      /* 0: none */
+    const float *sinks;  /* [Hq] or NULL */
 } problem;
 
 int oracle_num_threads(void) {
@@ -66,7 +77,16 @@ static int check_problem(const problem *p) {
         p->max_pages <= 0 || p->num_pages <= 0 || p->q_len <= 0)
         return 1;
     if (p->Hq % p->Hkv != 0) return 1;
+    if (p->window < 0 || p->softcap < 0.0) return 1;
     return 0;
+}
+
+/* First key row (b, i) may see: the window's lower end, or 0. */
+static int64_t first_key(const problem *p, int b, int i) {
+    int64_t pos = (int64_t)p->lens[b] - p->q_len + i;
+    if (p->window <= 0) return 0;
+    int64_t lo = pos - p->window + 1;
+    return lo > 0 ? lo : 0;
 }
 
 /* Split a flat row index r = (b * Hq + h) * q_len + i into its parts. */
@@ -94,7 +114,9 @@ static const float *kv_row(const problem *p, const float *pool, int b, int g, in
 static double score(const problem *p, const float *qrow, const float *krow) {
     double acc = 0.0;
     for (int d = 0; d < p->D; ++d) acc += (double)qrow[d] * (double)krow[d];
-    return p->scale * acc;
+    double s = p->scale * acc;
+    if (p->softcap > 0.0) s = p->softcap * tanh(s / p->softcap);
+    return s;
 }
 
 /*
@@ -105,10 +127,10 @@ static double score(const problem *p, const float *qrow, const float *krow) {
 int oracle_attn(const float *q, const float *k_pages, const float *v_pages,
                 const int32_t *page_table, const int32_t *seq_lens,
                 int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
-                int q_len, double scale, const int64_t *rows, int64_t n_rows,
-                double *out, double *lse) {
+                int q_len, double scale, int window, double softcap, const float *sinks,
+                const int64_t *rows, int64_t n_rows, double *out, double *lse) {
     problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
-                 max_pages, num_pages, q_len, scale};
+                 max_pages, num_pages, q_len, scale, window, softcap, sinks};
     if (check_problem(&p)) return 1;
     int64_t total = rows ? n_rows : (int64_t)B * Hq * q_len;
     int G = Hq / Hkv;
@@ -138,10 +160,11 @@ int oracle_attn(const float *q, const float *k_pages, const float *v_pages,
             err = 4;
             continue;
         }
-        /* scores and their maximum */
+        const int64_t lo = first_key(&p, b, i);
+        /* scores of the visible keys lo..n-1 and their maximum (with the sink) */
         double M = -INFINITY;
         int bad = 0;
-        for (int64_t t = 0; t < n; ++t) {
+        for (int64_t t = lo; t < n; ++t) {
             const float *krow = kv_row(&p, k_pages, b, g, t);
             if (!krow) { bad = 1; break; }
             s[t] = score(&p, qrow, krow);
@@ -153,16 +176,18 @@ int oracle_attn(const float *q, const float *k_pages, const float *v_pages,
             err = 3;
             continue;
         }
+        if (sinks && (double)sinks[h] > M) M = (double)sinks[h];
         /* softmax weights and the weighted sum of value rows */
         double l = 0.0;
         double *o = out + j * D;
         for (int d = 0; d < D; ++d) o[d] = 0.0;
-        for (int64_t t = 0; t < n; ++t) {
+        for (int64_t t = lo; t < n; ++t) {
             double w = exp(s[t] - M);
             l += w;
             const float *vrow = kv_row(&p, v_pages, b, g, t);
             for (int d = 0; d < D; ++d) o[d] += w * (double)vrow[d];
         }
+        if (sinks) l += exp((double)sinks[h] - M); /* the sink has no value row */
         for (int d = 0; d < D; ++d) o[d] /= l;
         if (lse) lse[j] = M + log(l);
         free(s);
@@ -171,19 +196,20 @@ int oracle_attn(const float *q, const float *k_pages, const float *v_pages,
 }
 
 /*
- * The page-by-page fold: each page's keys update the running state
+ * The page-by-page fold: each page's visible keys update the running state
  *   m' = max(m, max_t s_t),  c = exp(m - m'),
  *   l' = c l + sum_t exp(s_t - m'),  acc' = c acc + sum_t exp(s_t - m') v_t
- * in logical page order; o = acc / l at the end.  Same argument convention as
- * oracle_attn.  Used only to check the fold against the full-KV definition.
+ * in logical page order; the sink, if any, is folded last as a key with no
+ * value; o = acc / l at the end.  Same argument convention as oracle_attn.
+ * Used only to check the fold against the full-KV definition.
  */
 int oracle_folded(const float *q, const float *k_pages, const float *v_pages,
                   const int32_t *page_table, const int32_t *seq_lens,
                   int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
-                  int q_len, double scale, const int64_t *rows, int64_t n_rows,
-                  double *out, double *lse) {
+                  int q_len, double scale, int window, double softcap, const float *sinks,
+                  const int64_t *rows, int64_t n_rows, double *out, double *lse) {
     problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
-                 max_pages, num_pages, q_len, scale};
+                 max_pages, num_pages, q_len, scale, window, softcap, sinks};
     if (check_problem(&p)) return 1;
     int64_t total = rows ? n_rows : (int64_t)B * Hq * q_len;
     int G = Hq / Hkv;
@@ -214,26 +240,28 @@ int oracle_folded(const float *q, const float *k_pages, const float *v_pages,
             err = 4;
             continue;
         }
+        const int64_t lo = first_key(&p, b, i);
         for (int d = 0; d < D; ++d) acc[d] = 0.0;
         double m = -INFINITY, l = 0.0;
         int bad = 0;
-        for (int64_t t0 = 0; t0 < n && !bad; t0 += P) {
-            int64_t cnt = n - t0 < P ? n - t0 : P;
+        for (int64_t pg = lo / P; pg * P < n && !bad; ++pg) {
+            int64_t t0 = pg * P > lo ? pg * P : lo;
+            int64_t t1 = pg * P + P < n ? pg * P + P : n;
             double m_page = -INFINITY;
-            for (int64_t u = 0; u < cnt; ++u) {
-                const float *krow = kv_row(&p, k_pages, b, g, t0 + u);
+            for (int64_t t = t0; t < t1; ++t) {
+                const float *krow = kv_row(&p, k_pages, b, g, t);
                 if (!krow) { bad = 1; break; }
-                s[u] = score(&p, qrow, krow);
-                if (s[u] > m_page) m_page = s[u];
+                s[t - t0] = score(&p, qrow, krow);
+                if (s[t - t0] > m_page) m_page = s[t - t0];
             }
             if (bad) break;
             double m_new = m_page > m ? m_page : m;
             double c = exp(m - m_new); /* exp(-inf) = 0 on the first page */
             l *= c;
             for (int d = 0; d < D; ++d) acc[d] *= c;
-            for (int64_t u = 0; u < cnt; ++u) {
-                double w = exp(s[u] - m_new);
-                const float *vrow = kv_row(&p, v_pages, b, g, t0 + u);
+            for (int64_t t = t0; t < t1; ++t) {
+                double w = exp(s[t - t0] - m_new);
+                const float *vrow = kv_row(&p, v_pages, b, g, t);
                 l += w;
                 for (int d = 0; d < D; ++d) acc[d] += w * (double)vrow[d];
             }
@@ -245,6 +273,14 @@ int oracle_folded(const float *q, const float *k_pages, const float *v_pages,
             err = 3;
             continue;
         }
+        if (sinks) {
+            double sk = (double)sinks[h];
+            double m_new = sk > m ? sk : m;
+            double cs = exp(m - m_new);
+            for (int d = 0; d < D; ++d) acc[d] *= cs;
+            l = l * cs + exp(sk - m_new);
+            m = m_new;
+        }
         for (int d = 0; d < D; ++d) acc[d] /= l;
         if (lse) lse[j] = m + log(l);
     }
@@ -254,15 +290,17 @@ int oracle_folded(const float *q, const float *k_pages, const float *v_pages,
 /*
  * Unnormalised softmax state of one row over the visible keys in
  * [t_begin, t_end): m = max s_t, l = sum exp(s_t - m), acc = sum exp(s_t - m) v_t.
- * An empty range gives m = -inf, l = 0, acc = 0.  One row per call (flat index r).
+ * Window and softcap apply; the sink does not (it is one more state: m = sink,
+ * l = 1, acc = 0).  An empty range gives m = -inf, l = 0, acc = 0.  One row per
+ * call (flat index r).
  */
 int oracle_state(const float *q, const float *k_pages, const float *v_pages,
                  const int32_t *page_table, const int32_t *seq_lens,
                  int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
-                 int q_len, double scale, int64_t r, int64_t t_begin, int64_t t_end,
-                 double *m_out, double *l_out, double *acc) {
+                 int q_len, double scale, int window, double softcap, int64_t r,
+                 int64_t t_begin, int64_t t_end, double *m_out, double *l_out, double *acc) {
     problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
-                 max_pages, num_pages, q_len, scale};
+                 max_pages, num_pages, q_len, scale, window, softcap, NULL};
     if (check_problem(&p)) return 1;
     if (r < 0 || r >= (int64_t)B * Hq * q_len) return 1;
     int b, h, i;
@@ -270,7 +308,8 @@ int oracle_state(const float *q, const float *k_pages, const float *v_pages,
     int g = h / (Hq / Hkv);
     int64_t n = visible_keys(&p, b, i);
     if (n < 0) return 2;
-    if (t_begin < 0) t_begin = 0;
+    int64_t lo = first_key(&p, b, i);
+    if (t_begin < lo) t_begin = lo;
     if (t_end > n) t_end = n;
     const float *qrow = q + r * D;
     double m = -INFINITY;

@@ -19,7 +19,11 @@ MUTANTS = {
     "pool_transposed": ("(((int64_t)page * p->Hkv + g) * p->P", "(((int64_t)g * p->num_pages + page) * p->P"),
     "page_index": ("p->table[(int64_t)b * p->max_pages + t / p->P]", "p->table[(int64_t)b * p->max_pages + t % p->max_pages]"),
     "dot_operand": ("(double)qrow[d] * (double)krow[d]", "(double)qrow[d] * (double)krow[0]"),
-    "scale_dropped": ("return p->scale * acc;", "return acc;"),
+    "scale_dropped": ("double s = p->scale * acc;", "double s = acc;"),
+    "window_off_by_one": ("int64_t lo = pos - p->window + 1;", "int64_t lo = pos - p->window;"),
+    "softcap_inside_scale": ("s = p->softcap * tanh(s / p->softcap);", "s = p->softcap * tanh(s);"),
+    "sink_sign": ("if (sinks) l += exp((double)sinks[h] - M);", "if (sinks) l += exp(M - (double)sinks[h]);"),
+    "fold_sink_dropped": ("l = l * cs + exp(sk - m_new);", "l = l * cs;"),
     "exp_sign": ("double w = exp(s[t] - M);", "double w = exp(M - s[t]);"),
     "normalise_dropped": ("for (int d = 0; d < D; ++d) o[d] /= l;", ""),
     "gqa_interleaved": ("int g = h / G;\n        int64_t n = visible_keys(&p, b, i);\n        if (n < 0) {\n#pragma omp atomic write\n            err = 2;\n            continue;\n        }\n        const float *qrow = q + r * D;\n        double *s = (double *)malloc",

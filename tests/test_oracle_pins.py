@@ -13,7 +13,11 @@ pages fix, never from re-running the oracle's own formula:
     (CPUAttn README, "Operator model");
   * a library routine on tiny shapes: torch's fp64 scaled_dot_product_attention
     with an explicit causal-offset mask;
-  * a hand-worked example stored under tests/golden/.
+  * a hand-worked example stored under tests/golden/;
+  * for the score/mask variants (window, softcap, sinks): the same brute force
+    with the variant applied, their limits (a window covering every key, a huge
+    cap, a sink at -1e4), closed forms (window 1; one key with a sink; q = 0 with
+    a sink), the sink as one more merge state, and torch SDPA with a band mask.
 """
 import json
 import math
@@ -45,8 +49,9 @@ def run_oracle(fn, q, k, v, lens, P, Hq, Hkv, scale, seed=3, **kw):
     return fn(q, kp, vp, table, np.asarray(lens, np.int32), Hq, Hkv, scale, **kw)
 
 
-def brute_force(q, k, v, lens, Hq, Hkv, scale, digits=50):
-    """Materialise s = scale * q k^T with the causal-suffix mask; softmax without shift."""
+def brute_force(q, k, v, lens, Hq, Hkv, scale, digits=50, window=0, softcap=0.0, sinks=None):
+    """Materialise s = scale * q k^T with the causal-suffix (and window) mask, apply the
+    softcap, softmax without shift with exp(sink) in the denominator."""
     mpmath.mp.dps = digits
     B, _, q_len, D = q.shape
     G = Hq // Hkv
@@ -57,17 +62,22 @@ def brute_force(q, k, v, lens, Hq, Hkv, scale, digits=50):
             g = h // G
             for i in range(q_len):
                 pos = L - q_len + i
-                w = []
+                w = {}
                 for t in range(L):
-                    if t > pos:
+                    if t > pos or (window and pos - t >= window):
                         continue
                     s = mpmath.mpf(0)
                     for d in range(D):
                         s += mpmath.mpf(float(q[b, h, i, d])) * mpmath.mpf(float(k[b, g, t, d]))
-                    w.append(mpmath.exp(mpmath.mpf(scale) * s))
-                z = mpmath.fsum(w)
+                    s = mpmath.mpf(scale) * s
+                    if softcap:
+                        s = mpmath.mpf(softcap) * mpmath.tanh(s / mpmath.mpf(softcap))
+                    w[t] = mpmath.exp(s)
+                z = mpmath.fsum(w.values())
+                if sinks is not None:
+                    z += mpmath.exp(mpmath.mpf(float(sinks[h])))
                 for d in range(D):
-                    num = mpmath.fsum(wt * mpmath.mpf(float(v[b, g, t, d])) for t, wt in enumerate(w))
+                    num = mpmath.fsum(wt * mpmath.mpf(float(v[b, g, t, d])) for t, wt in w.items())
                     out[b, h, i, d] = float(num / z)
     return out
 
@@ -275,3 +285,102 @@ def test_invalid_inputs_are_rejected():
         oracle.attn(q, kp, vp, table, np.asarray([9], np.int32), 2, 1, scale)
     with pytest.raises(oracle.OracleError):  # fewer keys than query rows
         oracle.attn(q, kp, vp, table, np.asarray([1], np.int32), 2, 1, scale)
+
+
+# ---------------------------------------------------------------- score / mask variants
+# (ferrox-core crate index: causal_gqa_attention_windowed, _softcap, _sinks)
+
+@pytest.mark.parametrize("variant", [
+    dict(window=3), dict(softcap=2.5), dict(sinks=[0.7, -1.2, 3.0, 0.0]),
+    dict(window=5, softcap=1.5, sinks=[-0.3, 2.0, 0.1, -4.0]),
+])
+def test_variants_brute_force_50_digits(variant):
+    B, Hq, Hkv, D, lens, q_len, P = 2, 4, 2, 3, [9, 6], 3, 2
+    q, k, v, scale = rand_problem(21, B, Hq, Hkv, D, lens, q_len, P, spread=1.8)
+    kw = dict(variant)
+    if "sinks" in kw:
+        kw["sinks"] = np.asarray(kw["sinks"], np.float32)
+    ref = brute_force(q, k, v, lens, Hq, Hkv, scale, **kw)
+    for fn in (oracle.attn, oracle.folded):
+        got = run_oracle(fn, q, k, v, lens, P, Hq, Hkv, scale, **kw)
+        np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_window_limits():
+    lens, q_len = [23, 11], 5
+    q, k, v, scale = rand_problem(22, 2, 2, 1, 8, lens, q_len, 4)
+    plain = run_oracle(oracle.attn, q, k, v, lens, 4, 2, 1, scale)
+    wide = run_oracle(oracle.attn, q, k, v, lens, 4, 2, 1, scale, window=23)
+    np.testing.assert_array_equal(plain, wide)  # a window covering every key changes nothing
+    one = run_oracle(oracle.attn, q, k, v, lens, 4, 2, 1, scale, window=1)
+    for b, L in enumerate(lens):           # window 1: only the row's own position
+        for i in range(q_len):
+            pos = L - q_len + i
+            for h in range(2):
+                assert np.array_equal(one[b, h, i], v[b, 0, pos].astype(np.float64))
+
+
+def test_softcap_limit_and_sink_limits():
+    lens = [30]
+    q, k, v, scale = rand_problem(23, 1, 2, 1, 8, lens, 4, 8, spread=2.0)
+    plain = run_oracle(oracle.attn, q, k, v, lens, 8, 2, 1, scale)
+    huge_cap = run_oracle(oracle.attn, q, k, v, lens, 8, 2, 1, scale, softcap=1e7)
+    np.testing.assert_allclose(huge_cap, plain, rtol=1e-9, atol=1e-12)
+    dead_sink = run_oracle(oracle.attn, q, k, v, lens, 8, 2, 1, scale,
+                           sinks=np.float32([-1e4, -1e4]))
+    np.testing.assert_array_equal(dead_sink, plain)  # exp(-1e4) is 0 in fp64
+
+
+def test_sink_closed_forms():
+    # one visible key with score s and a sink sigma: o = v / (1 + exp(sigma - s))
+    q = np.float32([[[[1.0, 0.0]]]])
+    k = np.float32([[[[0.75, 3.0]]]])
+    v = np.float32([[[[2.0, -6.0]]]])
+    out = run_oracle(oracle.attn, q, k, v, [1], 1, 1, 1, 1.0, sinks=np.float32([1.25]))
+    np.testing.assert_allclose(out[0, 0, 0],
+                               v[0, 0, 0].astype(np.float64) / (1.0 + math.exp(1.25 - 0.75)),
+                               rtol=1e-15)
+    # q = 0: n equal weights and the sink: o = mean(v) * n / (n + exp(sigma))
+    L = 7
+    _, k, v, scale = rand_problem(24, 1, 1, 1, 5, [L], 1, 4)
+    q = np.zeros((1, 1, 1, 5), np.float32)
+    out = run_oracle(oracle.attn, q, k, v, [L], 4, 1, 1, scale, sinks=np.float32([0.5]))
+    expect = v[0, 0, :L].astype(np.float64).mean(0) * L / (L + math.exp(0.5))
+    np.testing.assert_allclose(out[0, 0, 0], expect, rtol=1e-14)
+
+
+def test_sink_is_one_more_merge_state_and_window_splits():
+    L, W = 60, 37
+    q, k, v, scale = rand_problem(25, 1, 2, 1, 16, [L], 1, 8, spread=1.3)
+    kp, vp, table = page_kv(k, v, [L], 8, seed=5)
+    lens = np.asarray([L], np.int32)
+    sinks = np.float32([0.9, -0.4])
+    full, full_lse = oracle.attn(q, kp, vp, table, lens, 2, 1, scale, want_lse=True,
+                                 window=W, softcap=3.0, sinks=sinks)
+    for row in range(2):
+        parts = [oracle.state(q, kp, vp, table, lens, 2, 1, scale, row, a, b_,
+                              window=W, softcap=3.0)
+                 for a, b_ in ((0, 20), (20, 41), (41, 60))]
+        ms = [p_[0] for p_ in parts] + [float(sinks[row])]
+        ls = [p_[1] for p_ in parts] + [1.0]
+        accs = np.stack([p_[2] for p_ in parts] + [np.zeros(16)])
+        o, lse = oracle.merge(ms, ls, accs)
+        np.testing.assert_allclose(o, full.reshape(2, -1)[row], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(lse, full_lse.reshape(-1)[row], rtol=1e-14)
+
+
+def test_window_library_pin_torch_sdpa():
+    B, Hq, Hkv, D, lens, q_len, W = 2, 4, 2, 16, [40, 25], 6, 9
+    q, k, v, scale = rand_problem(26, B, Hq, Hkv, D, lens, q_len, 8)
+    got = run_oracle(oracle.attn, q, k, v, lens, 8, Hq, Hkv, scale, window=W)
+    for b in range(B):
+        L = lens[b]
+        qt = torch.from_numpy(q[b:b + 1]).double()
+        kt = torch.from_numpy(k[b:b + 1, :, :L]).double().repeat_interleave(2, dim=1)
+        vt = torch.from_numpy(v[b:b + 1, :, :L]).double().repeat_interleave(2, dim=1)
+        pos = torch.arange(q_len)[:, None] + (L - q_len)
+        t = torch.arange(L)[None, :]
+        mask = (t <= pos) & (pos - t < W)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
+                                                               scale=scale)
+        np.testing.assert_allclose(got[b], ref[0].numpy(), rtol=1e-12, atol=1e-13)
