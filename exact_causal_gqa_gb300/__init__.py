@@ -55,7 +55,9 @@ class _Launch(ctypes.Structure):
                 ("lse", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("status_word", ctypes.c_void_p),
                 ("stream", ctypes.c_void_p), ("split_tokens", ctypes.c_int32),
-                ("debug_flags", ctypes.c_uint32), ("events", ctypes.c_void_p)]
+                ("debug_flags", ctypes.c_uint32), ("events", ctypes.c_void_p),
+                ("window", ctypes.c_int32), ("softcap", ctypes.c_float),
+                ("sinks", ctypes.c_void_p)]
 
 
 _lib = None
@@ -100,7 +102,8 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 
 def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=None,
-            status=None, stream=None, split_tokens=0, debug_flags=0, events=None) -> _Launch:
+            status=None, stream=None, split_tokens=0, debug_flags=0, events=None,
+            window=0, softcap=0.0, sinks=None) -> _Launch:
     L = _Launch()
     L.batch, L.q_len = q.shape[0], q.shape[2]
     L.max_pages_per_seq = page_table.shape[1]
@@ -117,6 +120,9 @@ def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=Non
     L.split_tokens = split_tokens
     L.debug_flags = debug_flags
     L.events = events
+    L.window = window
+    L.softcap = softcap
+    L.sinks = _ptr(sinks)
     return L
 
 
@@ -139,9 +145,12 @@ def workspace_size(kind: str, q_shape, n_q_heads, n_kv_heads, head_dim, page_tok
 
 def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads,
           head_dim, page_tokens, scale, *, out=None, out_dtype=None, lse=None,
-          workspace=None, status=None, split_tokens=0, debug_flags=0, events=None):
+          workspace=None, status=None, split_tokens=0, debug_flags=0, events=None,
+          window=0, softcap=0.0, sinks=None):
     """``events``: optional ctypes array of three cudaEvent_t handles (see
-    EventTimer) recorded around the main kernel and the merge."""
+    EventTimer) recorded around the main kernel and the merge.  ``window``,
+    ``softcap`` and ``sinks`` (float32 CUDA tensor [n_q_heads]) select the score /
+    mask variants; the defaults give plain causal attention."""
     lib = load_library()
     for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
                     ("page_table", page_table), ("seq_lens", seq_lens)):
@@ -156,10 +165,14 @@ def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if status is not None and (status.dtype != torch.int32 or status.numel() < 1):
         raise ValueError("status must be an int32 device tensor")
+    if sinks is not None and (not sinks.is_cuda or sinks.dtype != torch.float32 or
+                              sinks.numel() != n_q_heads or not sinks.is_contiguous()):
+        raise ValueError("sinks must be a contiguous float32 CUDA tensor [n_q_heads]")
     stream = torch.cuda.current_stream(q.device).cuda_stream
     L = _launch(q, k_pages, page_table, out_dtype, out, lse, None, status, stream,
                 split_tokens, debug_flags,
-                None if events is None else ctypes.cast(events, ctypes.c_void_p).value)
+                None if events is None else ctypes.cast(events, ctypes.c_void_p).value,
+                window, softcap, sinks)
     need = lib.atlas_attn_workspace_size(_KINDS[kind], n_q_heads, n_kv_heads, head_dim,
                                          page_tokens, ctypes.byref(L))
     if workspace is None and 0 < need < ctypes.c_size_t(-1).value:

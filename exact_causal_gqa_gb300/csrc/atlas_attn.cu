@@ -199,6 +199,8 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         !aligned16(L->workspace))
         return ATLAS_ERR_INVALID_ARG;
     if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return ATLAS_ERR_INVALID_ARG;
+    if (L->window < 0 || !(L->softcap >= 0.f) || L->softcap == INFINITY)
+        return ATLAS_ERR_INVALID_ARG;
     Plan plan;
     atlas_status st = make_plan(kind, Hq, Hkv, D, P, L, &plan);
     if (st != ATLAS_OK) return st;
@@ -230,6 +232,9 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     sp.col_tiles = plan.col_tiles;
     sp.require_full = kind == ATLAS_KIND_PREFILL;
     sp.scale_log2 = scale * kLog2e;
+    sp.window = L->window;
+    sp.softcap_log2 = L->softcap > 0.f ? L->softcap * kLog2e : 0.f;
+    sp.softcap_inv = L->softcap > 0.f ? scale / L->softcap : 0.f;
     sp.ws_acc = static_cast<float *>(L->workspace);
     sp.ws_ml = reinterpret_cast<float *>(static_cast<char *>(L->workspace) + plan.ml_offset);
     sp.status = L->status_word;
@@ -268,6 +273,10 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         tp.hilo_below = fabsf(scale) * sqrtf((float)D) > kHiLoScale ? INT32_MAX : kHiLoBelow;
         tp.negate_scores = scale < 0.f;
         tp.scale_log2 = fabsf(scale) * kLog2e;
+        tp.window = L->window;
+        tp.softcap_log2 = L->softcap > 0.f ? L->softcap * kLog2e : 0.f;
+        tp.softcap_inv = L->softcap > 0.f ? fabsf(scale) / L->softcap : 0.f;
+        tp.sinks = L->sinks;
         tp.out = L->out;
         tp.out_bf16 = L->out_dtype == ATLAS_BF16;
         tp.lse = L->lse;
@@ -308,6 +317,8 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     mp.chunk = plan.chunk;
     mp.n_chunks = plan.n_chunks;
     mp.require_full = sp.require_full;
+    mp.window = L->window;
+    mp.sinks = L->sinks;
     mp.ws_acc = sp.ws_acc;
     mp.ws_ml = sp.ws_ml;
     mp.out = L->out;

@@ -192,12 +192,16 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         return;  // split mode: the merge writes NaN rows for this sequence
     }
     const int kv_hi = L - p.q_len + i_max + 1;   // keys the tiles' last row sees
-    const int kv_min = L - p.q_len + i_min + 1;  // keys their first row sees
-    int kv_begin = 0, kv_end = kv_hi;
+    // Keys the tiles' first row sees (its window may cut that short).
+    const int kv_min = p.window > 0 ? min(L - p.q_len + i_min + 1, p.window)
+                                    : L - p.q_len + i_min + 1;
+    // Blocks below every row's window are skipped whole.
+    const int kv_lo = p.window > 0 ? max(0, L - p.q_len + i_min + 1 - p.window) / BN * BN : 0;
+    int kv_begin = kv_lo, kv_end = kv_hi;
     if (p.split) {
-        kv_begin = c * p.chunk;
-        if (kv_begin >= kv_hi) return;
-        kv_end = min(kv_hi, kv_begin + p.chunk);
+        kv_begin = max(c * p.chunk, kv_lo);
+        kv_end = min(kv_hi, c * p.chunk + p.chunk);
+        if (kv_begin >= kv_end) return;
     }
     const int nb = (kv_end - kv_begin + BN - 1) / BN;
     {
@@ -445,6 +449,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         const bool valid = f < rows_unit;
         const int i = valid ? f % p.q_len : 0;
         const int lim_row = valid ? min(L - p.q_len + i + 1, kv_end) : 0;
+        const int lo_row = (valid && p.window > 0) ? max(0, L - p.q_len + i + 1 - p.window) : 0;
+        const bool capped = p.softcap_log2 > 0.f;
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
         const uint32_t to = tl + C::o_col(x);
         float m_used = -INFINITY, l = 0.f;
@@ -459,8 +465,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             if (r == 0) TRACE(2 + x, 2, j);
             tc_fence_after();
             const uint32_t ts = tl + C::s_col(x, bsel);
-            const int nvis = lim_row - (kv_begin + j * BN);  // visible columns of this row
-            const bool all_visible = __all_sync(0xffffffffu, nvis >= BN);
+            const int nvis = lim_row - (kv_begin + j * BN);  // visible columns: [nlo, nvis)
+            const int nlo = lo_row - (kv_begin + j * BN);
+            const bool all_visible = __all_sync(0xffffffffu, nvis >= BN && nlo <= 0);
             // Pass 1: row max of the raw scores (scale_log2 >= 0, so the scaled
             // maximum is the maximum scaled), four chains of 3-input max.
             // Outer loops stay rolled: a fully unrolled body overflows the
@@ -486,14 +493,20 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         const int col = cc * 32 + e;
-                        const float v0 = col < nvis ? __uint_as_float(sr[e]) : -INFINITY;
-                        const float v1 = col + 1 < nvis ? __uint_as_float(sr[e + 1]) : -INFINITY;
+                        const float v0 =
+                            col < nvis && col >= nlo ? __uint_as_float(sr[e]) : -INFINITY;
+                        const float v1 = col + 1 < nvis && col + 1 >= nlo
+                                             ? __uint_as_float(sr[e + 1])
+                                             : -INFINITY;
                         m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], v0, v1);
                     }
                 }
             }
             const float mraw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;
+            // the softcap is increasing, so it maps the raw maximum to the maximum
+            const float mx = mraw == -INFINITY ? -INFINITY
+                             : capped ? p.softcap_log2 * tanh_acc(mraw * p.softcap_inv)
+                                      : mraw * p.scale_log2;
             float corr = 1.f;
             if (mx > m_used + kRescaleThreshold) {
                 corr = ex2(m_used - mx);  // 0 on the first visible block
@@ -515,16 +528,24 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             // has been read already.  The remainder goes 32 columns further on, so
             // with the split the two quarters of a half are read before writing.
             auto quarter = [&](const uint32_t (&sr)[32], int cc, uint32_t (&hw)[16],
-                               uint32_t (&lw)[16], bool masked, bool split) {
+                               uint32_t (&lw)[16], bool masked, bool split, bool cap) {
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    float2 t = ffma2(make_float2(__uint_as_float(sr[2 * k]),
-                                                 __uint_as_float(sr[2 * k + 1])),
-                                     sc2, nm2);
+                    float2 t;
+                    if (cap) {
+                        t.x = p.softcap_log2 * tanh_acc(__uint_as_float(sr[2 * k]) *
+                                                        p.softcap_inv) - mref;
+                        t.y = p.softcap_log2 * tanh_acc(__uint_as_float(sr[2 * k + 1]) *
+                                                        p.softcap_inv) - mref;
+                    } else {
+                        t = ffma2(make_float2(__uint_as_float(sr[2 * k]),
+                                              __uint_as_float(sr[2 * k + 1])),
+                                  sc2, nm2);
+                    }
                     if (masked) {
                         const int c0 = cc * 32 + 2 * k;
-                        t.x = c0 < nvis ? t.x : -INFINITY;
-                        t.y = c0 + 1 < nvis ? t.y : -INFINITY;
+                        t.x = c0 < nvis && c0 >= nlo ? t.x : -INFINITY;
+                        t.y = c0 + 1 < nvis && c0 + 1 >= nlo ? t.y : -INFINITY;
                     }
                     const float2 e2 = make_float2(ex2(t.x), ex2(t.y));
                     rs2[k & 3] = fadd2(rs2[k & 3], e2);
@@ -536,13 +557,13 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     }
                 }
             };
-            if (!hilo && all_visible) {
+            if (!hilo && all_visible && !capped) {
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t sr[32], hw[16], lw[16];
                     tmem_ld32(ts + cc * 32, sr);
                     tmem_wait_ld();
-                    quarter(sr, cc, hw, lw, false, false);
+                    quarter(sr, cc, hw, lw, false, false, false);
                     tmem_st16(ts + (cc >> 1) * 64 + (cc & 1) * 16, hw);
                 }
             } else {
@@ -552,10 +573,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     tmem_ld32(ts + h * 64, sr0);
                     tmem_ld32(ts + h * 64 + 32, sr1);
                     tmem_wait_ld();
-                    quarter(sr0, 2 * h, hw, lw, !all_visible, hilo);
+                    quarter(sr0, 2 * h, hw, lw, !all_visible, hilo, capped);
                     tmem_st16(ts + h * 64, hw);
                     if (hilo) tmem_st16(ts + h * 64 + 32, lw);
-                    quarter(sr1, 2 * h + 1, hw, lw, !all_visible, hilo);
+                    quarter(sr1, 2 * h + 1, hw, lw, !all_visible, hilo, capped);
                     tmem_st16(ts + h * 64 + 16, hw);
                     if (hilo) tmem_st16(ts + h * 64 + 48, lw);
                 }
@@ -597,8 +618,18 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         // ---------------------------------------------------- epilogue
         tc_fence_after();
         if (ok) {
-            const float inv = 1.f / l;
             const int64_t row = tile_row(p, b, hkv, valid ? f : 0);
+            // Direct mode folds the sink (one more state: m = sink log2 e, l = 1,
+            // acc = 0) here; split mode leaves it to the merge.
+            float osc = 1.f;  // factor on acc
+            if (!p.split && p.sinks && valid) {
+                const float sink2 = p.sinks[(row / p.q_len) % p.Hq] * kLog2e;
+                const float M = fmaxf(m_used, sink2);
+                osc = ex2(m_used - M);
+                l = l * osc + ex2(sink2 - M);
+                m_used = M;
+            }
+            const float inv = osc / l;
             const int64_t slot = row * p.n_chunks + c;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {

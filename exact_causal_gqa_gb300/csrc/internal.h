@@ -33,6 +33,9 @@ struct SplitParams {
     int32_t col_tiles;          // ceil(G*q_len / columns per CTA)
     int32_t require_full;       // prefill: seq_len must equal q_len
     float scale_log2;           // scale * log2(e)
+    int32_t window;             // > 0: keys pos - window < t <= pos only
+    float softcap_log2;         // > 0: s2 = softcap_log2 * tanh(raw * softcap_inv)
+    float softcap_inv;          // scale / softcap
     float *ws_acc;              // [B*Hq*q_len][n_chunks][D]   unnormalised accumulators
     float *ws_ml;               // [B*Hq*q_len][n_chunks][2]   (m in log2 units, l)
     uint32_t *status;           // may be null
@@ -42,6 +45,8 @@ struct SplitParams {
 struct MergeParams {
     const int32_t *seq_lens;
     int32_t B, Hq, D, q_len, max_pages, P, chunk, n_chunks, require_full;
+    int32_t window;             // splits below a row's window hold nothing for it
+    const float *sinks;         // [Hq] natural-log logits or null: one more state (m, 1, 0)
     const float *ws_acc;
     const float *ws_ml;
     void *out;
@@ -65,6 +70,10 @@ struct TcParams {
     int32_t hilo_below;       // tiles whose rows see fewer keys use a hi+lo split of P
     int32_t negate_scores;    // scale < 0: S = -Q K^T with |scale| (keeps the max exact)
     float scale_log2;         // |scale| * log2(e)
+    int32_t window;           // > 0: keys pos - window < t <= pos only
+    float softcap_log2;       // > 0: s2 = softcap_log2 * tanh(raw * softcap_inv)
+    float softcap_inv;        // |scale| / softcap
+    const float *sinks;       // [Hq] or null (direct mode folds it into the epilogue)
     void *out;
     int32_t out_bf16;
     float *lse;

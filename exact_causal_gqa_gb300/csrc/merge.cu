@@ -33,26 +33,31 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) merge_kernel(const MergePara
     bool nan_row = bad_len;
     if (!bad_len) {
         const int visible = L - p.q_len + i + 1;
+        // splits holding this row's keys: [first, nsplit)
+        const int first = p.window > 0 ? max(0, visible - p.window) / p.chunk : 0;
         const int nsplit = (visible + p.chunk - 1) / p.chunk;
         const float *ml = p.ws_ml + row * p.n_chunks * 2;
-        float M = -INFINITY;
+        // A sink is one more state: m = sink * log2(e), l = 1, acc = 0.
+        const float sink2 =
+            p.sinks ? p.sinks[(row / p.q_len) % p.Hq] * kLog2e : -INFINITY;
+        float M = sink2;
         bool has_nan = false;
-        for (int s = lane; s < nsplit; s += 32) {
+        for (int s = first + lane; s < nsplit; s += 32) {
             const float m = ml[2 * s], l = ml[2 * s + 1];
             if (isnan(l) || isnan(m)) has_nan = true;
             else if (l > 0.f) M = fmaxf(M, m);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        has_nan = __any_sync(0xffffffffu, has_nan);
+        has_nan = __any_sync(0xffffffffu, has_nan) || isnan(sink2);
         nan_row = has_nan || M == -INFINITY;
         if (!nan_row) {
             float acc[DPL];
 #pragma unroll
             for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
-            float lsum = 0.f;
+            float lsum = p.sinks ? ex2(sink2 - M) : 0.f;
             const float *wa = p.ws_acc + row * p.n_chunks * D + lane * DPL;
-            for (int s = 0; s < nsplit; ++s) {
+            for (int s = first; s < nsplit; ++s) {
                 const float m = ml[2 * s], l = ml[2 * s + 1];
                 const float w = l > 0.f ? ex2(m - M) : 0.f;
                 lsum = fmaf(w, l, lsum);

@@ -209,6 +209,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // MUFU base-2 exponential (ex2.approx.ftz.f32); exp2(-inf) = +0.
+__device__ __forceinline__ float ex2(float x);
+
+// tanh(x) = sign(x) (1 - e) / (1 + e), e = exp(-2|x|), from the MUFU exp2 and a
+// fast divide: absolute error ~1e-7 (the MUFU tanh.approx is only ~2^-11).
+__device__ __forceinline__ float tanh_acc(float x) {
+    const float e = ex2(-2.8853900817779268f * fabsf(x));  // -2 log2(e) |x|
+    return copysignf(__fdividef(1.f - e, 1.f + e), x);
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

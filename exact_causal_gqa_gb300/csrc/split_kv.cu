@@ -48,6 +48,17 @@ __device__ __forceinline__ int column_visible(const SplitParams &p, int L, int n
     return L - p.q_len + (n % p.q_len) + 1;
 }
 
+// First key column n may see: the lower end of its window, or 0.
+__device__ __forceinline__ int column_first(const SplitParams &p, int L, int n) {
+    return p.window > 0 ? max(0, column_visible(p, L, n) - p.window) : 0;
+}
+
+// Score in log2 units from a raw dot product: scale (and the softcap, if any).
+__device__ __forceinline__ float score_log2(const SplitParams &p, float raw) {
+    return p.softcap_log2 > 0.f ? p.softcap_log2 * tanh_acc(raw * p.softcap_inv)
+                                : raw * p.scale_log2;
+}
+
 // Shared prologue: decides whether this CTA has work.  Returns false when the
 // CTA must exit (nothing visible, or an error that has been recorded).
 template <int NCOLS>
@@ -63,12 +74,17 @@ __device__ bool split_prologue(const SplitParams &p, int &L, int &kv_begin, int 
     }
     col0 = ct * NCOLS;
     ncols = min(NCOLS, p.G * p.q_len - col0);
-    int i_max = 0;
-    for (int c = 0; c < ncols; ++c) i_max = max(i_max, (col0 + c) % p.q_len);
+    int i_max = 0, i_min = p.q_len;
+    for (int c = 0; c < ncols; ++c) {
+        i_max = max(i_max, (col0 + c) % p.q_len);
+        i_min = min(i_min, (col0 + c) % p.q_len);
+    }
     const int kv_hi = L - p.q_len + i_max + 1;
-    kv_begin = blockIdx.x * p.chunk;
-    if (kv_begin >= kv_hi) return false;
-    kv_end = min(kv_hi, kv_begin + p.chunk);
+    // Keys below every column's window are skipped whole (64-key blocks).
+    const int kv_lo = p.window > 0 ? max(0, L - p.q_len + i_min + 1 - p.window) : 0;
+    kv_begin = max((int)blockIdx.x * p.chunk, kv_lo / kSplitBlockTokens * kSplitBlockTokens);
+    kv_end = min(kv_hi, (int)blockIdx.x * p.chunk + p.chunk);
+    if (kv_begin >= kv_end) return false;
 
     // Every page id this split will touch must be inside the pool.
     const int pg0 = kv_begin / p.P, pg1 = (kv_end - 1) / p.P;
@@ -254,14 +270,16 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
                 qf[kk][nt][1] = qrow ? *reinterpret_cast<const uint32_t *>(qrow + d0 + 8) : 0u;
             }
         }
-        // Key limit of each of this thread's score columns (0 for padding columns).
-        int lim[NT][2];
+        // Visible key range [lo, lim) of each of this thread's score columns
+        // (empty for padding columns).
+        int lim[NT][2], lo[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int c = nt * 8 + 2 * (lane % 4) + e;
                 lim[nt][e] = c < ncols ? min(kv_end, column_visible(p, L, col0 + c)) : 0;
+                lo[nt][e] = c < ncols ? column_first(p, L, col0 + c) : 0;
                 m_run[nt][e] = -INFINITY;
                 l_run[nt][e] = 0.f;
             }
@@ -313,7 +331,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int key = key0 + lane / 4 + 8 * (e >> 1);
-                        sc[nt][e] = key < lim[nt][e & 1] ? sc[nt][e] * p.scale_log2 : -INFINITY;
+                        sc[nt][e] = key < lim[nt][e & 1] && key >= lo[nt][e & 1]
+                                        ? score_log2(p, sc[nt][e])
+                                        : -INFINITY;
                     }
 #pragma unroll
                     for (int ce = 0; ce < 2; ++ce) {
@@ -439,7 +459,7 @@ __global__ void __launch_bounds__(128)
     const float *vp = static_cast<const float *>(p.v_pages);
 
     float qv[NC][DPL], accv[NC][DPL], m_run[NC], l_run[NC];
-    int lim[NC];
+    int lim[NC], lo[NC];
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         const bool ok = c < ncols;
@@ -452,6 +472,7 @@ __global__ void __launch_bounds__(128)
             accv[c][j] = 0.f;
         }
         lim[c] = ok ? min(kv_end, column_visible(p, L, col0 + c)) : 0;
+        lo[c] = ok ? column_first(p, L, col0 + c) : 0;
         m_run[c] = -INFINITY;
         l_run[c] = 0.f;
     }
@@ -479,13 +500,13 @@ __global__ void __launch_bounds__(128)
             const int t = t0 + u;
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-                if (t >= lim[c]) continue;  // warp-uniform (lim <= kv_end)
+                if (t >= lim[c] || t < lo[c]) continue;  // warp-uniform (lim <= kv_end)
                 float dot = 0.f;
 #pragma unroll
                 for (int j = 0; j < DPL; ++j) dot = fmaf(qv[c][j], kr[u][j], dot);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                const float s2 = dot * p.scale_log2;
+                const float s2 = score_log2(p, dot);
                 const float m_new = fmaxf(m_run[c], s2);
                 const float corr = ex2(m_run[c] - m_new);
                 const float pw = ex2(s2 - m_new);

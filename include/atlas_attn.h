@@ -13,6 +13,10 @@
  *                  s_t = scale * <q[b][h][i], k_t>,  M = max_t s_t
  *   lse[b][h][i] = M + ln sum_{t <= pos} exp(s_t - M)     (natural log)
  *
+ * with the optional variants of atlas_launch: a window keeps only keys
+ * t > pos - window, a softcap c replaces s_t by c tanh(s_t / c), and a sink
+ * logit adds exp(sink[h] - M) to both denominators (M then covers it too).
+ *
  * Sources (page title, section):
  *   CFR-Atlas README, "Core contract": folding exact pages into an online-softmax
  *     state gives the full-KV result, which is what is computed here;
@@ -109,6 +113,13 @@ typedef struct {
     void *const *events;       /* optional host array of 3 cudaEvent_t, recorded on
                                   `stream` before the main kernel, between it and the
                                   merge, and after the merge (profiling); NULL = none */
+    /* Score / mask variants (ferrox-core: causal_gqa_attention_windowed, _softcap,
+     * _sinks).  All zero / NULL gives plain causal attention. */
+    int32_t window;            /* > 0: row i sees only keys pos - window < t <= pos */
+    float softcap;             /* > 0: each scaled score s becomes softcap*tanh(s/softcap) */
+    const float *sinks;        /* optional device [n_q_heads]: a logit per q head that joins
+                                  the softmax denominator (natural-log units, like the
+                                  scaled scores) with no value row; lse includes it */
 } atlas_launch;
 
 /*

@@ -20,10 +20,11 @@ BF16_ABS = 2e-3
 BF16_STORE_REL = 2.0 ** -8
 
 
-def oracle_rows(prob, rows=None, want_lse=False):
+def oracle_rows(prob, rows=None, want_lse=False, **variants):
+    """The oracle on the problem's host bytes; ``variants``: window, softcap, sinks."""
     return oracle.attn(prob.q, prob.k_pages, prob.v_pages, prob.page_table, prob.seq_lens,
                        prob.n_q_heads, prob.n_kv_heads, prob.scale, rows=rows,
-                       want_lse=want_lse)
+                       want_lse=want_lse, **variants)
 
 
 def run_gpu(prob_dev, out_dtype=None, **kw):
