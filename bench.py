@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling captures)")
+    ap.add_argument("--window", type=int, default=0, help="sliding window (keys); 0 = none")
+    ap.add_argument("--softcap", type=float, default=0.0, help="logit softcap; 0 = none")
+    ap.add_argument("--sinks", action="store_true", help="one sink logit per q head")
     return ap.parse_args()
 
 
@@ -87,13 +90,22 @@ def peaks():
     return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
 
 
-def work_of(prob):
-    """Algorithmic work of one call: (KV bytes, FLOPs)."""
-    kv = prob.kv_bytes()
+def work_of(prob, window: int = 0):
+    """Algorithmic work of one call: (KV bytes, FLOPs).  KV bytes count each key
+    any query row of a sequence may see once (K and V); FLOPs count 4*D per
+    (query row, visible key) -- QK^T and PV, masked keys excluded."""
     lens = prob.seq_lens.to(torch.int64).cpu()
     sq = prob.q_len
-    # keys seen by query rows: sum_b sum_i (L_b - sq + i + 1)
-    keys = int((lens * sq).sum()) - sq * (sq - 1) // 2 * prob.batch
+    elem = prob.k_pages.element_size()
+    if window > 0:
+        kv_keys = int(torch.clamp(lens, max=window + sq - 1).sum())
+        i = torch.arange(sq, dtype=torch.int64)
+        vis = (lens[:, None] - sq + i[None, :] + 1).clamp(max=window)
+        keys = int(vis.sum())
+    else:
+        kv_keys = int(lens.sum())
+        keys = int((lens * sq).sum()) - sq * (sq - 1) // 2 * prob.batch
+    kv = 2 * kv_keys * prob.n_kv_heads * prob.head_dim * elem
     flops = 4 * prob.head_dim * prob.n_q_heads * keys
     return kv, flops
 
@@ -197,13 +209,17 @@ def run_atlas(args, world, rank, local):
     seed = rank_seed(args.config, rank)
     overrides = {"B": args.batch} if args.batch else {}
     prob = inputs.make_config(args.config, seed=seed, device=dev, **overrides)
-    kv_bytes, flops = work_of(prob)
+    kv_bytes, flops = work_of(prob, args.window)
+    variants = dict(window=args.window, softcap=args.softcap)
+    if args.sinks:
+        g = torch.Generator().manual_seed(seed)
+        variants["sinks"] = (torch.randn(prob.n_q_heads, generator=g) * 2.0).float().to(dev)
     out_dtype = torch.bfloat16 if prob.out_dtype == "bf16" else torch.float32
     out = torch.empty(prob.q.shape, dtype=out_dtype, device=dev)
     ws_bytes = atlas.workspace_size(prob.kind, prob.q.shape, prob.n_q_heads, prob.n_kv_heads,
                                     prob.head_dim, prob.page_tokens, prob.max_pages,
                                     prob.num_pages, dtype=prob.q.dtype, out_dtype=out_dtype,
-                                    split_tokens=args.split_tokens)
+                                    split_tokens=args.split_tokens, window=args.window)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     timers = [atlas.EventTimer() for _ in range(args.steps)]
@@ -212,7 +228,7 @@ def run_atlas(args, world, rank, local):
 
     def step(timer=None):
         atlas.run(prob, out=out, workspace=ws, status=status, split_tokens=args.split_tokens,
-                  events=None if timer is None else timer.handles)
+                  events=None if timer is None else timer.handles, **variants)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -268,7 +284,7 @@ def run_atlas(args, world, rank, local):
                 d.copy_(h, non_blocking=True)
             atlas._call(prob.kind, *dbuf, prob.n_q_heads, prob.n_kv_heads, prob.head_dim,
                         prob.page_tokens, prob.scale, out=out, workspace=ws, status=status,
-                        split_tokens=args.split_tokens)
+                        split_tokens=args.split_tokens, **variants)
             host_out.copy_(out, non_blocking=True)
 
         for _ in range(2):
@@ -325,7 +341,9 @@ def run_atlas(args, world, rank, local):
         "dtype": prob.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
         "config": {
-            "workload": cfg["name"] if not args.batch else f'{cfg["name"]} (batch {args.batch})',
+            "workload": cfg["name"] + (f" (batch {args.batch})" if args.batch else "") +
+            (f" window {args.window}" if args.window else "") +
+            (f" softcap {args.softcap}" if args.softcap else "") + (" sinks" if args.sinks else ""),
             "kind": prob.kind, "batch": prob.batch, "n_q_heads": prob.n_q_heads,
             "n_kv_heads": prob.n_kv_heads, "head_dim": prob.head_dim,
             "page_tokens": prob.page_tokens, "q_len": prob.q_len,
@@ -335,6 +353,7 @@ def run_atlas(args, world, rank, local):
                    else f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB KV vs 129 MB)"),
             "parallelism": f"replicas x{world} (independent batches per GPU)",
             "split_tokens": args.split_tokens or "auto",
+            "variants": {"window": args.window, "softcap": args.softcap, "sinks": args.sinks},
             "per_step_ms": {"min": round(min(step_ms), 5),
                             "median": round(statistics.median(step_ms), 5)},
             "main_kernel_ms": round(main_avg, 5),

@@ -128,9 +128,10 @@ def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=Non
 
 def workspace_size(kind: str, q_shape, n_q_heads, n_kv_heads, head_dim, page_tokens,
                    max_pages_per_seq, num_pages, dtype=torch.bfloat16,
-                   out_dtype=None, split_tokens=0) -> int:
-    """Workspace bytes a call needs (from shapes only)."""
+                   out_dtype=None, split_tokens=0, window=0) -> int:
+    """Workspace bytes a call needs (from shapes, split size and window only)."""
     L = _Launch()
+    L.window = window
     L.batch, L.q_len = q_shape[0], q_shape[2]
     L.max_pages_per_seq, L.num_pages = max_pages_per_seq, num_pages
     L.q_dtype = L.kv_dtype = _DTYPES.get(dtype, -1)

@@ -8,6 +8,7 @@
 #include <limits.h>
 #include <math.h>
 #include <stdint.h>
+#include <algorithm>
 #include <mutex>
 
 namespace atlas {
@@ -88,6 +89,11 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     }
     const int64_t max_ctx = (int64_t)L->max_pages_per_seq * P;
     if (max_ctx > INT32_MAX / 2) return ATLAS_ERR_INVALID_ARG;
+    // Keys one (sequence, kv head) may need: a window bounds them.  Splits are
+    // sized from this; the split count still covers the whole context (splits
+    // below every row's window exit at once).
+    const int64_t work_ctx =
+        L->window > 0 ? std::min(max_ctx, (int64_t)L->window + L->q_len + 127) : max_ctx;
     if ((int64_t)L->num_pages * Hkv * P >= INT32_MAX) return ATLAS_ERR_INVALID_ARG;
     if (L->q_len > max_ctx) return ATLAS_ERR_INVALID_ARG;
     if (L->split_tokens < 0 || L->split_tokens % kSplitBlockTokens != 0)
@@ -109,7 +115,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         if (L->split_tokens > 0) {
             chunk = round_up(L->split_tokens, 128);
         } else if (tiles < kTcDirectTiles && !(L->debug_flags & ATLAS_DEBUG_TC_DIRECT)) {
-            chunk = round_up((max_ctx * tiles + kTcPlanCtas - 1) / kTcPlanCtas, 128);
+            chunk = round_up((work_ctx * tiles + kTcPlanCtas - 1) / kTcPlanCtas, 128);
             if (chunk < 1024) chunk = 1024;
             if (chunk > 8192) chunk = 8192;
         }
@@ -139,7 +145,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     int64_t chunk = L->split_tokens;
     if (chunk == 0) {
         const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
-        chunk = round_up((max_ctx * units + kPlanCtas - 1) / kPlanCtas, kSplitBlockTokens);
+        chunk = round_up((work_ctx * units + kPlanCtas - 1) / kPlanCtas, kSplitBlockTokens);
         // The f32 kernel has no pipeline to fill: small splits just add CTAs.
         const int64_t min_chunk = plan->path == Path::SplitF32 ? kSplitBlockTokens : 512;
         if (chunk > kMaxSplit) chunk = kMaxSplit;

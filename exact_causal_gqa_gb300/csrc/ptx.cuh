@@ -211,11 +211,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // MUFU base-2 exponential (ex2.approx.ftz.f32); exp2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x);
 
-// tanh(x) = sign(x) (1 - e) / (1 + e), e = exp(-2|x|), from the MUFU exp2 and a
-// fast divide: absolute error ~1e-7 (the MUFU tanh.approx is only ~2^-11).
+// tanh(x) = 2 / (1 + exp(-2x)) - 1 from the MUFU exp2 and reciprocal: absolute
+// error ~1e-7, saturating correctly at both ends (the MUFU tanh.approx is only
+// good to ~2^-11 relative, too coarse for a logit cap).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float tanh_acc(float x) {
-    const float e = ex2(-2.8853900817779268f * fabsf(x));  // -2 log2(e) |x|
-    return copysignf(__fdividef(1.f - e, 1.f + e), x);
+    const float e = ex2(-2.8853900817779268f * x);  // exp(-2x) = 2^(-2 log2(e) x)
+    return fmaf(2.f, rcp_approx(1.f + e), -1.f);    // rcp(inf) = 0 -> -1
 }
 
 __device__ __forceinline__ float ex2(float x) {
