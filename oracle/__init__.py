@@ -60,8 +60,10 @@ def _load():
         common = [P, P, P, P, P, I, I, I, I, I, I, I, I, Dd, I, Dd]
         for name in ("oracle_attn", "oracle_folded"):
             fn = getattr(lib, name)
-            fn.argtypes = common + [P, P, L, P, P]
+            fn.argtypes = common + [P, P, P, L, P, P]
             fn.restype = I
+        lib.oracle_kv_append.argtypes = [P] * 7 + [I] * 7
+        lib.oracle_kv_append.restype = I
         lib.oracle_state.argtypes = common + [L, L, L, P, P, P]
         lib.oracle_state.restype = I
         lib.oracle_merge.argtypes = [I, I, P, P, P, P, P]
@@ -118,7 +120,7 @@ def _prepare(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads):
 
 
 def _run(name, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scale,
-         rows=None, want_lse=False, window=0, softcap=0.0, sinks=None):
+         rows=None, want_lse=False, window=0, softcap=0.0, sinks=None, q_lens=None):
     lib = _load()
     q, k, v, table, lens, dims = _prepare(q, k_pages, v_pages, page_table, seq_lens,
                                           n_q_heads, n_kv_heads)
@@ -126,6 +128,9 @@ def _run(name, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads,
     sinks_arr = None if sinks is None else _f32(sinks)
     if sinks_arr is not None and sinks_arr.shape != (Hq,):
         raise OracleError("sinks must hold one logit per q head")
+    qlen_arr = None if q_lens is None else _i32(q_lens)
+    if qlen_arr is not None and qlen_arr.shape != (B,):
+        raise OracleError("q_lens must hold one count per sequence")
     if rows is None:
         n_rows = B * Hq * q_len
         rows_arr = None
@@ -137,6 +142,7 @@ def _run(name, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads,
     rc = getattr(lib, name)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(table), _ptr(lens), *dims, float(scale),
         int(window), float(softcap), _ptr(sinks_arr) if sinks_arr is not None else None,
+        _ptr(qlen_arr) if qlen_arr is not None else None,
         _ptr(rows_arr) if rows_arr is not None else None, n_rows,
         _ptr(out), _ptr(lse) if lse is not None else None)
     if rc:
@@ -149,25 +155,27 @@ def _run(name, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads,
 
 
 def attn(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scale,
-         rows=None, want_lse=False, window=0, softcap=0.0, sinks=None):
+         rows=None, want_lse=False, window=0, softcap=0.0, sinks=None, q_lens=None):
     """Full-KV causal GQA attention in fp64.
 
     q[B][Hq][q_len][D]; pools [num_pages][Hkv][P][D]; page_table[B][max_pages];
     seq_lens[B].  Query row i of sequence b sits at position seq_lens[b] - q_len + i
     and sees keys 0..that position (only the last ``window`` of them when window > 0);
     ``softcap`` c > 0 maps each scaled score s to c tanh(s / c); ``sinks`` (one logit
-    per q head) adds exp(sink) to the softmax denominator.  ``rows`` (flat indices
+    per q head) adds exp(sink) to the softmax denominator.  ``q_lens`` (ragged query
+    counts, <= q_len) makes row i of sequence b a query only when i < q_lens[b], at
+    position seq_lens[b] - q_lens[b] + i (padding rows: 0, lse NaN).  ``rows`` (flat indices
     (b*Hq+h)*q_len+i) restricts the output to those rows, returned as [len(rows)][D].
     """
     return _run("oracle_attn", q, k_pages, v_pages, page_table, seq_lens, n_q_heads,
-                n_kv_heads, scale, rows, want_lse, window, softcap, sinks)
+                n_kv_heads, scale, rows, want_lse, window, softcap, sinks, q_lens)
 
 
 def folded(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scale,
-           rows=None, want_lse=False, window=0, softcap=0.0, sinks=None):
+           rows=None, want_lse=False, window=0, softcap=0.0, sinks=None, q_lens=None):
     """The same result reached by folding one page at a time into (m, l, acc)."""
     return _run("oracle_folded", q, k_pages, v_pages, page_table, seq_lens, n_q_heads,
-                n_kv_heads, scale, rows, want_lse, window, softcap, sinks)
+                n_kv_heads, scale, rows, want_lse, window, softcap, sinks, q_lens)
 
 
 def state(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, scale,
@@ -201,3 +209,22 @@ def merge(ms, ls, accs):
     if rc:
         raise OracleError(f"oracle_merge: {_ERRORS.get(rc, rc)}")
     return out, float(lse[0])
+
+
+def kv_append(k_new, v_new, k_pages, v_pages, page_table, seq_lens, n_new=None):
+    """Write new K/V rows [B][Hkv][max_new][D] of each sequence to the page slots of
+    positions seq_lens[b] .. seq_lens[b] + n_new[b] - 1.  Returns new float64-exact
+    float32 pools (the inputs are not modified)."""
+    lib = _load()
+    kn, vn = _f32(k_new), _f32(v_new)
+    kp, vp = _f32(k_pages).copy(), _f32(v_pages).copy()
+    table, lens = _i32(page_table), _i32(seq_lens)
+    nn = None if n_new is None else _i32(n_new)
+    B, Hkv, max_new, D = kn.shape
+    num_pages, _, P, _ = kp.shape
+    rc = lib.oracle_kv_append(_ptr(kn), _ptr(vn), _ptr(kp), _ptr(vp), _ptr(table), _ptr(lens),
+                              _ptr(nn) if nn is not None else None, B, Hkv, max_new, D, P,
+                              table.shape[1], num_pages)
+    if rc:
+        raise OracleError(f"oracle_kv_append: {_ERRORS.get(rc, rc)}")
+    return kp, vp

@@ -39,6 +39,15 @@
  *                  value row: l += exp(sink[h] - M), M = max(M, sink[h]).
  * W = 0, c = 0 and sinks == NULL give plain attention.
  *
+ * Ragged query counts (chunked prefill): with q_lens != NULL sequence b has
+ * q_lens[b] <= q_len query rows, the last q_lens[b] positions of its K/V; rows
+ * i >= q_lens[b] are padding (output 0, lse NaN).
+ *
+ * oracle_kv_append is the write before all of this: the new tokens' K and V rows
+ * of each sequence go to the page slots of positions seq_lens[b] .. (CFR-Atlas
+ * README, "Minimal integration": row-major K[token][dim] per (layer, kv head,
+ * range); ferrox-core "cache" module: a KV cache growable one position at a time).
+ *
  * All inputs are fp32 arrays holding the exact stored values (bf16 inputs are
  * widened exactly by the caller); all arithmetic is fp64.
  *
@@ -62,6 +71,7 @@ typedef struct {
     int window;          /* 0: none */
     double softcap;      /* 0: none */
     const float *sinks;  /* [Hq] or NULL */
+    const int32_t *q_lens; /* [B] query rows per sequence (<= q_len) or NULL */
 } problem;
 
 int oracle_num_threads(void) {
@@ -71,6 +81,9 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Query rows of sequence b: q_lens[b] when given (ragged), else q_len. */
+static int rows_of(const problem *p, int b) { return p->q_lens ? p->q_lens[b] : p->q_len; }
 
 static int check_problem(const problem *p) {
     if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->P <= 0 ||
@@ -83,7 +96,7 @@ static int check_problem(const problem *p) {
 
 /* First key row (b, i) may see: the window's lower end, or 0. */
 static int64_t first_key(const problem *p, int b, int i) {
-    int64_t pos = (int64_t)p->lens[b] - p->q_len + i;
+    int64_t pos = (int64_t)p->lens[b] - rows_of(p, b) + i;
     if (p->window <= 0) return 0;
     int64_t lo = pos - p->window + 1;
     return lo > 0 ? lo : 0;
@@ -100,7 +113,7 @@ static void row_parts(const problem *p, int64_t r, int *b, int *h, int *i) {
 static int64_t visible_keys(const problem *p, int b, int i) {
     int64_t L = p->lens[b];
     if (L > (int64_t)p->max_pages * p->P) return -1;
-    int64_t n = L - p->q_len + i + 1;
+    int64_t n = L - rows_of(p, b) + i + 1;
     return n >= 1 ? n : -1;
 }
 
@@ -128,9 +141,10 @@ int oracle_attn(const float *q, const float *k_pages, const float *v_pages,
                 const int32_t *page_table, const int32_t *seq_lens,
                 int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
                 int q_len, double scale, int window, double softcap, const float *sinks,
-                const int64_t *rows, int64_t n_rows, double *out, double *lse) {
+                const int32_t *q_lens, const int64_t *rows, int64_t n_rows, double *out,
+                double *lse) {
     problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
-                 max_pages, num_pages, q_len, scale, window, softcap, sinks};
+                 max_pages, num_pages, q_len, scale, window, softcap, sinks, q_lens};
     if (check_problem(&p)) return 1;
     int64_t total = rows ? n_rows : (int64_t)B * Hq * q_len;
     int G = Hq / Hkv;
@@ -147,6 +161,16 @@ int oracle_attn(const float *q, const float *k_pages, const float *v_pages,
         }
         row_parts(&p, r, &b, &h, &i);
         int g = h / G;
+        if (q_lens && (q_lens[b] < 0 || q_lens[b] > q_len)) {
+#pragma omp atomic write
+            err = 1;
+            continue;
+        }
+        if (i >= rows_of(&p, b)) { /* padding row of a ragged batch: not a query */
+            for (int d = 0; d < D; ++d) out[j * D + d] = 0.0;
+            if (lse) lse[j] = NAN;
+            continue;
+        }
         int64_t n = visible_keys(&p, b, i);
         if (n < 0) {
 #pragma omp atomic write
@@ -207,9 +231,10 @@ int oracle_folded(const float *q, const float *k_pages, const float *v_pages,
                   const int32_t *page_table, const int32_t *seq_lens,
                   int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
                   int q_len, double scale, int window, double softcap, const float *sinks,
-                  const int64_t *rows, int64_t n_rows, double *out, double *lse) {
+                  const int32_t *q_lens, const int64_t *rows, int64_t n_rows, double *out,
+                  double *lse) {
     problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
-                 max_pages, num_pages, q_len, scale, window, softcap, sinks};
+                 max_pages, num_pages, q_len, scale, window, softcap, sinks, q_lens};
     if (check_problem(&p)) return 1;
     int64_t total = rows ? n_rows : (int64_t)B * Hq * q_len;
     int G = Hq / Hkv;
@@ -226,6 +251,16 @@ int oracle_folded(const float *q, const float *k_pages, const float *v_pages,
         }
         row_parts(&p, r, &b, &h, &i);
         int g = h / G;
+        if (q_lens && (q_lens[b] < 0 || q_lens[b] > q_len)) {
+#pragma omp atomic write
+            err = 1;
+            continue;
+        }
+        if (i >= rows_of(&p, b)) {
+            for (int d = 0; d < D; ++d) out[j * D + d] = 0.0;
+            if (lse) lse[j] = NAN;
+            continue;
+        }
         int64_t n = visible_keys(&p, b, i);
         if (n < 0) {
 #pragma omp atomic write
@@ -300,7 +335,7 @@ int oracle_state(const float *q, const float *k_pages, const float *v_pages,
                  int q_len, double scale, int window, double softcap, int64_t r,
                  int64_t t_begin, int64_t t_end, double *m_out, double *l_out, double *acc) {
     problem p = {q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, P,
-                 max_pages, num_pages, q_len, scale, window, softcap, NULL};
+                 max_pages, num_pages, q_len, scale, window, softcap, NULL, NULL};
     if (check_problem(&p)) return 1;
     if (r < 0 || r >= (int64_t)B * Hq * q_len) return 1;
     int b, h, i;
@@ -353,5 +388,36 @@ int oracle_merge(int S, int D, const double *m, const double *l, const double *a
     }
     for (int d = 0; d < D; ++d) out[d] /= L;
     if (lse) *lse = M + log(L);
+    return 0;
+}
+
+/*
+ * Append: for each sequence b, kv head g and new token j < n_new[b] (n_new == NULL:
+ * all max_new), write k_new[b][g][j][:] (and v_new) to the page slot of position
+ * t = seq_lens[b] + j:  pools[page_table[b][t / P]][g][t % P][:].  Pools are
+ * float32 here.  Returns 3 for a page id outside the pool, 2 for a position past
+ * the page table.
+ */
+int oracle_kv_append(const float *k_new, const float *v_new, float *k_pages, float *v_pages,
+                     const int32_t *page_table, const int32_t *seq_lens, const int32_t *n_new,
+                     int B, int Hkv, int max_new, int D, int P, int max_pages, int num_pages) {
+    for (int b = 0; b < B; ++b) {
+        int cnt = n_new ? n_new[b] : max_new;
+        if (cnt < 0 || cnt > max_new) return 1;
+        for (int j = 0; j < cnt; ++j) {
+            int64_t t = (int64_t)seq_lens[b] + j;
+            if (t >= (int64_t)max_pages * P) return 2;
+            int32_t page = page_table[(int64_t)b * max_pages + t / P];
+            if (page < 0 || page >= num_pages) return 3;
+            for (int g = 0; g < Hkv; ++g) {
+                const int64_t src = (((int64_t)b * Hkv + g) * max_new + j) * D;
+                const int64_t dst = (((int64_t)page * Hkv + g) * P + t % P) * D;
+                for (int d = 0; d < D; ++d) {
+                    k_pages[dst + d] = k_new[src + d];
+                    v_pages[dst + d] = v_new[src + d];
+                }
+            }
+        }
+    }
     return 0;
 }

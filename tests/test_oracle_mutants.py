@@ -13,8 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle_attn.c")
 
 MUTANTS = {
-    "causal_off_by_one": ("int64_t n = L - p->q_len + i + 1;", "int64_t n = L - p->q_len + i;"),
-    "causal_reversed": ("int64_t n = L - p->q_len + i + 1;", "int64_t n = L - i;"),
+    "causal_off_by_one": ("int64_t n = L - rows_of(p, b) + i + 1;", "int64_t n = L - rows_of(p, b) + i;"),
+    "causal_reversed": ("int64_t n = L - rows_of(p, b) + i + 1;", "int64_t n = L - i;"),
     "slot_index": ("* p->P + t % p->P) * p->D;", "* p->P + (t + 1) % p->P) * p->D;"),
     "pool_transposed": ("(((int64_t)page * p->Hkv + g) * p->P", "(((int64_t)g * p->num_pages + page) * p->P"),
     "page_index": ("p->table[(int64_t)b * p->max_pages + t / p->P]", "p->table[(int64_t)b * p->max_pages + t % p->max_pages]"),
@@ -24,10 +24,12 @@ MUTANTS = {
     "softcap_inside_scale": ("s = p->softcap * tanh(s / p->softcap);", "s = p->softcap * tanh(s);"),
     "sink_sign": ("if (sinks) l += exp((double)sinks[h] - M);", "if (sinks) l += exp(M - (double)sinks[h]);"),
     "fold_sink_dropped": ("l = l * cs + exp(sk - m_new);", "l = l * cs;"),
+    "ragged_position": ("int64_t n = L - rows_of(p, b) + i + 1;", "int64_t n = L - p->q_len + i + 1;"),
+    "append_slot": ("const int64_t dst = (((int64_t)page * Hkv + g) * P + t % P) * D;",
+                    "const int64_t dst = (((int64_t)page * Hkv + g) * P + j % P) * D;"),
     "exp_sign": ("double w = exp(s[t] - M);", "double w = exp(M - s[t]);"),
     "normalise_dropped": ("for (int d = 0; d < D; ++d) o[d] /= l;", ""),
-    "gqa_interleaved": ("int g = h / G;\n        int64_t n = visible_keys(&p, b, i);\n        if (n < 0) {\n#pragma omp atomic write\n            err = 2;\n            continue;\n        }\n        const float *qrow = q + r * D;\n        double *s = (double *)malloc",
-                        "int g = h % p.Hkv;\n        int64_t n = visible_keys(&p, b, i);\n        if (n < 0) {\n#pragma omp atomic write\n            err = 2;\n            continue;\n        }\n        const float *qrow = q + r * D;\n        double *s = (double *)malloc"),
+    "gqa_interleaved": ("int g = h / G;\n        if (q_lens", "int g = h % p.Hkv;\n        if (q_lens"),
     "fold_rescale_dropped": ("l *= c;", ""),
     "fold_rescale_sign": ("double c = exp(m - m_new);", "double c = exp(m_new - m);"),
     "merge_weight_dropped": ("L += w * l[s];", "L += l[s];"),

@@ -384,3 +384,52 @@ def test_window_library_pin_torch_sdpa():
         ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
                                                                scale=scale)
         np.testing.assert_allclose(got[b], ref[0].numpy(), rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- ragged queries, append
+
+def test_ragged_rows_equal_each_sequence_alone_and_brute_force():
+    B, Hq, Hkv, D, q_len = 3, 4, 2, 6, 7
+    lens, q_lens = [20, 9, 7], [7, 3, 1]
+    q, k, v, scale = rand_problem(27, B, Hq, Hkv, D, lens, q_len, 4, spread=1.4)
+    got = run_oracle(oracle.attn, q, k, v, lens, 4, Hq, Hkv, scale, q_lens=q_lens)
+    for b in range(B):
+        qn = q_lens[b]
+        alone = run_oracle(oracle.attn, q[b:b + 1, :, :qn], k[b:b + 1], v[b:b + 1], [lens[b]],
+                           4, Hq, Hkv, scale)
+        np.testing.assert_allclose(got[b, :, :qn], alone[0], rtol=1e-14, atol=1e-15)
+        ref = brute_force(q[b:b + 1, :, :qn], k[b:b + 1], v[b:b + 1], [lens[b]], Hq, Hkv, scale)
+        np.testing.assert_allclose(got[b, :, :qn], ref[0], rtol=1e-13, atol=1e-14)
+        assert np.all(got[b, :, qn:] == 0.0)  # padding rows are not queries
+
+
+def test_append_then_gather_is_concatenation():
+    from tests.paging import gather_kv
+    rng = np.random.default_rng(28)
+    B, Hkv, D, P = 3, 2, 8, 4
+    old, new = [5, 8, 0], [3, 1, 6]
+    max_new = max(new)
+    total = [o + n for o, n in zip(old, new)]
+    k_log = rng.standard_normal((B, Hkv, max(total), D)).astype(np.float32)
+    v_log = rng.standard_normal((B, Hkv, max(total), D)).astype(np.float32)
+    # pages sized for the final lengths, filled with the old tokens only
+    kp, vp, table = page_kv(k_log, v_log, total, P, seed=6)
+    for b in range(B):
+        for t in range(old[b], total[b]):
+            phys = table[b, t // P]
+            kp[phys, :, t % P] = np.nan
+            vp[phys, :, t % P] = np.nan
+    k_new = np.zeros((B, Hkv, max_new, D), np.float32)
+    v_new = np.zeros((B, Hkv, max_new, D), np.float32)
+    for b in range(B):
+        k_new[b, :, :new[b]] = k_log[b, :, old[b]:total[b]]
+        v_new[b, :, :new[b]] = v_log[b, :, old[b]:total[b]]
+    kp2, vp2 = oracle.kv_append(k_new, v_new, kp, vp, table, np.int32(old), np.int32(new))
+    kg, vg = gather_kv(kp2, vp2, table, total)
+    for b in range(B):
+        np.testing.assert_array_equal(kg[b, :, :total[b]], k_log[b, :, :total[b]])
+        np.testing.assert_array_equal(vg[b, :, :total[b]], v_log[b, :, :total[b]])
+    bad = table.copy()
+    bad[0, 1] = kp.shape[0]
+    with pytest.raises(oracle.OracleError):
+        oracle.kv_append(k_new, v_new, kp, vp, bad, np.int32(old), np.int32(new))
