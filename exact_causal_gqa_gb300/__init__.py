@@ -11,6 +11,7 @@ Functions (same names as the C entry points):
   decode(...)   one query row per sequence            -> atlas_attn_decode
   suffix(...)   the last q_len positions as queries   -> atlas_attn_suffix
   prefill(...)  causal self-attention of a prompt     -> atlas_attn_prefill
+  kv_append(...)  new tokens' K/V into their pages    -> atlas_kv_append
   workspace_size(kind, ...)                            -> atlas_attn_workspace_size
   run_host(kind, ...)  host tensors in, host tensor out (copies on the stream)
 """
@@ -24,7 +25,7 @@ import torch
 
 from . import _build
 
-__all__ = ["AtlasError", "decode", "suffix", "prefill", "workspace_size", "run_host",
+__all__ = ["AtlasError", "decode", "suffix", "prefill", "kv_append", "workspace_size", "run_host",
            "library_path", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
            "DEBUG_WITHHOLD_STAGE", "KIND_DECODE", "KIND_SUFFIX", "KIND_PREFILL"]
 
@@ -57,7 +58,14 @@ class _Launch(ctypes.Structure):
                 ("stream", ctypes.c_void_p), ("split_tokens", ctypes.c_int32),
                 ("debug_flags", ctypes.c_uint32), ("events", ctypes.c_void_p),
                 ("window", ctypes.c_int32), ("softcap", ctypes.c_float),
-                ("sinks", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("q_lens", ctypes.c_void_p)]
+
+
+class _Append(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("max_new", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int), ("status_word", ctypes.c_void_p),
+                ("stream", ctypes.c_void_p)]
 
 
 _lib = None
@@ -87,6 +95,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.atlas_attn_workspace_size.argtypes = [ctypes.c_int] + [ctypes.c_int32] * 4 + [
         ctypes.POINTER(_Launch)]
     lib.atlas_attn_workspace_size.restype = ctypes.c_size_t
+    lib.atlas_kv_append.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int32] * 3 + [
+        ctypes.POINTER(_Append)]
+    lib.atlas_kv_append.restype = ctypes.c_int
     lib.atlas_attn_status_string.argtypes = [ctypes.c_int]
     lib.atlas_attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -103,7 +114,7 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=None,
             status=None, stream=None, split_tokens=0, debug_flags=0, events=None,
-            window=0, softcap=0.0, sinks=None) -> _Launch:
+            window=0, softcap=0.0, sinks=None, q_lens=None) -> _Launch:
     L = _Launch()
     L.batch, L.q_len = q.shape[0], q.shape[2]
     L.max_pages_per_seq = page_table.shape[1]
@@ -123,6 +134,7 @@ def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=Non
     L.window = window
     L.softcap = softcap
     L.sinks = _ptr(sinks)
+    L.q_lens = _ptr(q_lens)
     return L
 
 
@@ -147,11 +159,12 @@ def workspace_size(kind: str, q_shape, n_q_heads, n_kv_heads, head_dim, page_tok
 def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads,
           head_dim, page_tokens, scale, *, out=None, out_dtype=None, lse=None,
           workspace=None, status=None, split_tokens=0, debug_flags=0, events=None,
-          window=0, softcap=0.0, sinks=None):
+          window=0, softcap=0.0, sinks=None, q_lens=None):
     """``events``: optional ctypes array of three cudaEvent_t handles (see
     EventTimer) recorded around the main kernel and the merge.  ``window``,
     ``softcap`` and ``sinks`` (float32 CUDA tensor [n_q_heads]) select the score /
-    mask variants; the defaults give plain causal attention."""
+    mask variants; the defaults give plain causal attention.  ``q_lens`` (int32
+    CUDA tensor [B]) makes the batch ragged: sequence b has q_lens[b] query rows."""
     lib = load_library()
     for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
                     ("page_table", page_table), ("seq_lens", seq_lens)):
@@ -169,11 +182,14 @@ def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_
     if sinks is not None and (not sinks.is_cuda or sinks.dtype != torch.float32 or
                               sinks.numel() != n_q_heads or not sinks.is_contiguous()):
         raise ValueError("sinks must be a contiguous float32 CUDA tensor [n_q_heads]")
+    if q_lens is not None and (not q_lens.is_cuda or q_lens.dtype != torch.int32 or
+                               q_lens.numel() != q.shape[0]):
+        raise ValueError("q_lens must be an int32 CUDA tensor [batch]")
     stream = torch.cuda.current_stream(q.device).cuda_stream
     L = _launch(q, k_pages, page_table, out_dtype, out, lse, None, status, stream,
                 split_tokens, debug_flags,
                 None if events is None else ctypes.cast(events, ctypes.c_void_p).value,
-                window, softcap, sinks)
+                window, softcap, sinks, q_lens)
     need = lib.atlas_attn_workspace_size(_KINDS[kind], n_q_heads, n_kv_heads, head_dim,
                                          page_tokens, ctypes.byref(L))
     if workspace is None and 0 < need < ctypes.c_size_t(-1).value:
@@ -216,6 +232,34 @@ def run(problem, **kw):
     return fn(problem.q, problem.k_pages, problem.v_pages, problem.page_table,
               problem.seq_lens, problem.n_q_heads, problem.n_kv_heads, problem.head_dim,
               problem.page_tokens, problem.scale, **kw)
+
+
+def kv_append(k_new, v_new, k_pages, v_pages, page_table, seq_lens, n_new=None,
+              status=None):
+    """Write the new tokens' K/V rows [B][Hkv][max_new][D] of each sequence into its
+    pages at positions seq_lens[b] .. seq_lens[b] + n_new[b] - 1 (atlas_kv_append).
+    The pools are updated in place; seq_lens is not advanced."""
+    lib = load_library()
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("k_pages", k_pages),
+                    ("v_pages", v_pages), ("page_table", page_table), ("seq_lens", seq_lens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k_new.shape != v_new.shape or k_new.dim() != 4 or k_pages.dim() != 4:
+        raise ValueError("k_new/v_new must be [B][Hkv][max_new][D], pools [pages][Hkv][P][D]")
+    if k_new.dtype != k_pages.dtype:
+        raise ValueError("new rows and pools must share a dtype")
+    A = _Append()
+    A.batch, A.max_new = k_new.shape[0], k_new.shape[2]
+    A.max_pages_per_seq, A.num_pages = page_table.shape[1], k_pages.shape[0]
+    A.kv_dtype = _DTYPES.get(k_pages.dtype, -1)
+    A.status_word = _ptr(status)
+    A.stream = torch.cuda.current_stream(k_new.device).cuda_stream
+    rc = lib.atlas_kv_append(k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(),
+                             v_pages.data_ptr(), page_table.data_ptr(), seq_lens.data_ptr(),
+                             _ptr(n_new), k_new.shape[1], k_new.shape[3], k_pages.shape[2],
+                             ctypes.byref(A))
+    if rc != 0:
+        raise AtlasError(rc, status_string(rc))
 
 
 class EventTimer:

@@ -239,6 +239,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     sp.require_full = kind == ATLAS_KIND_PREFILL;
     sp.scale_log2 = scale * kLog2e;
     sp.window = L->window;
+    sp.q_lens = L->q_lens;
     sp.softcap_log2 = L->softcap > 0.f ? L->softcap * kLog2e : 0.f;
     sp.softcap_inv = L->softcap > 0.f ? scale / L->softcap : 0.f;
     sp.ws_acc = static_cast<float *>(L->workspace);
@@ -283,6 +284,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         tp.softcap_log2 = L->softcap > 0.f ? L->softcap * kLog2e : 0.f;
         tp.softcap_inv = L->softcap > 0.f ? fabsf(scale) / L->softcap : 0.f;
         tp.sinks = L->sinks;
+        tp.q_lens = L->q_lens;
         tp.out = L->out;
         tp.out_bf16 = L->out_dtype == ATLAS_BF16;
         tp.lse = L->lse;
@@ -325,6 +327,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     mp.require_full = sp.require_full;
     mp.window = L->window;
     mp.sinks = L->sinks;
+    mp.q_lens = L->q_lens;
     mp.ws_acc = sp.ws_acc;
     mp.ws_ml = sp.ws_ml;
     mp.out = L->out;
@@ -363,6 +366,45 @@ atlas_status atlas_attn_prefill(const void *q, const void *k_pages, const void *
                                 int32_t page_tokens, float scale, const atlas_launch *L) {
     return atlas::run(ATLAS_KIND_PREFILL, q, k_pages, v_pages, page_table, seq_lens, n_q_heads,
                       n_kv_heads, head_dim, page_tokens, scale, L);
+}
+
+atlas_status atlas_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
+                             const int32_t *page_table, const int32_t *seq_lens,
+                             const int32_t *n_new, int32_t n_kv_heads, int32_t head_dim,
+                             int32_t page_tokens, const atlas_append *A) {
+    if (!A || !k_new || !v_new || !k_pages || !v_pages || !page_table || !seq_lens)
+        return ATLAS_ERR_INVALID_ARG;
+    if (A->batch < 1 || A->max_pages_per_seq < 1 || A->num_pages < 1 || A->max_new < 0 ||
+        n_kv_heads < 1)
+        return ATLAS_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return ATLAS_ERR_UNSUPPORTED;
+    if (page_tokens < 1 || page_tokens > 128 || (page_tokens & (page_tokens - 1)))
+        return ATLAS_ERR_UNSUPPORTED;
+    if (A->kv_dtype != ATLAS_F32 && A->kv_dtype != ATLAS_BF16) return ATLAS_ERR_UNSUPPORTED;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+                          reinterpret_cast<uintptr_t>(k_pages) | reinterpret_cast<uintptr_t>(v_pages);
+    if (mis & 15u) return ATLAS_ERR_INVALID_ARG;
+    if (A->max_new == 0) return ATLAS_OK;
+    atlas::AppendParams ap{};
+    ap.k_new = k_new;
+    ap.v_new = v_new;
+    ap.k_pages = k_pages;
+    ap.v_pages = v_pages;
+    ap.page_table = page_table;
+    ap.seq_lens = seq_lens;
+    ap.n_new = n_new;
+    ap.B = A->batch;
+    ap.Hkv = n_kv_heads;
+    ap.max_new = A->max_new;
+    ap.P = page_tokens;
+    ap.max_pages = A->max_pages_per_seq;
+    ap.num_pages = A->num_pages;
+    ap.row_bytes = head_dim * (A->kv_dtype == ATLAS_BF16 ? 2 : 4);
+    ap.status = A->status_word;
+    (void)cudaGetLastError();
+    return atlas::launch_kv_append(ap, static_cast<cudaStream_t>(A->stream)) == cudaSuccess
+               ? ATLAS_OK
+               : ATLAS_ERR_CUDA;
 }
 
 size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,

@@ -174,23 +174,30 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         }
     }
     const int b = u / p.Hkv, hkv = u % p.Hkv;
-    const int L = p.seq_lens[b];
+    const int seq_len = p.seq_lens[b];
+    const int qn = p.q_lens ? p.q_lens[b] : p.q_len;  // query rows of this sequence
     const int rows_unit = p.G * p.q_len;
     // Both tiles cover the same prompt rows, so their key ranges agree.
     const int f0 = t0 * BM;
     const int f_last = min(f0 + BM, rows_unit) - 1;
     const bool spans = (f_last / p.q_len) != (f0 / p.q_len);
-    const int i_max = spans ? p.q_len - 1 : f_last % p.q_len;
     const int i_min = spans ? 0 : f0 % p.q_len;
 
-    if (L < p.q_len || L > p.max_pages * p.P || (p.require_full && L != p.q_len)) {
+    if (qn < 0 || qn > p.q_len || seq_len < qn || seq_len > p.max_pages * p.P ||
+        (p.require_full && seq_len != qn)) {
         if (threadIdx.x == 0 && c == 0 && p.status) atomicOr(p.status, ATLAS_DEV_BAD_SEQLEN);
+        const int rows_valid = (qn >= 0 && qn <= p.q_len) ? qn : p.q_len;
         if (!p.split && threadIdx.x < NT * BM) {
             const int f = (t0 + (int)(threadIdx.x / BM) * tstep) * BM + threadIdx.x % BM;
-            if (f < rows_unit) nan_row(p, b, hkv, f);
+            if (f < rows_unit && f % p.q_len < rows_valid) nan_row(p, b, hkv, f);
         }
         return;  // split mode: the merge writes NaN rows for this sequence
     }
+    if (i_min >= qn) return;  // only padding rows of a ragged sequence
+    // Last real row of the tiles; with L shifted by q_len - qn, row i sits at
+    // position L - q_len + i = seq_len - qn + i as in a full batch.
+    const int i_max = min(spans ? p.q_len - 1 : f_last % p.q_len, qn - 1);
+    const int L = seq_len - qn + p.q_len;
     const int kv_hi = L - p.q_len + i_max + 1;   // keys the tiles' last row sees
     // Keys the tiles' first row sees (its window may cut that short).
     const int kv_min = p.window > 0 ? min(L - p.q_len + i_min + 1, p.window)
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             if (threadIdx.x == 0 && p.status) atomicOr(p.status, ATLAS_DEV_BAD_PAGE);
             if (threadIdx.x < NT * BM) {
                 const int f = (t0 + (int)(threadIdx.x / BM) * tstep) * BM + threadIdx.x % BM;
-                if (f < rows_unit) {
+                if (f < rows_unit && f % p.q_len < qn) {
                     if (!p.split) {
                         nan_row(p, b, hkv, f);
                     } else {
@@ -446,7 +453,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         const int q4 = warp % 4;                      // TMEM lane quadrant
         const int r = q4 * 32 + lane;
         const int f = (t0 + x * tstep) * BM + r;
-        const bool valid = f < rows_unit;
+        const bool valid = f < rows_unit && f % p.q_len < qn;  // padding rows are not queries
         const int i = valid ? f % p.q_len : 0;
         const int lim_row = valid ? min(L - p.q_len + i + 1, kv_end) : 0;
         const int lo_row = (valid && p.window > 0) ? max(0, L - p.q_len + i + 1 - p.window) : 0;

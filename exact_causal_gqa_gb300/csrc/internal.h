@@ -36,6 +36,7 @@ struct SplitParams {
     int32_t window;             // > 0: keys pos - window < t <= pos only
     float softcap_log2;         // > 0: s2 = softcap_log2 * tanh(raw * softcap_inv)
     float softcap_inv;          // scale / softcap
+    const int32_t *q_lens;      // [B] ragged query rows (<= q_len) or null
     float *ws_acc;              // [B*Hq*q_len][n_chunks][D]   unnormalised accumulators
     float *ws_ml;               // [B*Hq*q_len][n_chunks][2]   (m in log2 units, l)
     uint32_t *status;           // may be null
@@ -47,6 +48,7 @@ struct MergeParams {
     int32_t B, Hq, D, q_len, max_pages, P, chunk, n_chunks, require_full;
     int32_t window;             // splits below a row's window hold nothing for it
     const float *sinks;         // [Hq] natural-log logits or null: one more state (m, 1, 0)
+    const int32_t *q_lens;      // [B] ragged query rows or null; padding rows untouched
     const float *ws_acc;
     const float *ws_ml;
     void *out;
@@ -74,12 +76,23 @@ struct TcParams {
     float softcap_log2;       // > 0: s2 = softcap_log2 * tanh(raw * softcap_inv)
     float softcap_inv;        // |scale| / softcap
     const float *sinks;       // [Hq] or null (direct mode folds it into the epilogue)
+    const int32_t *q_lens;    // [B] ragged query rows (<= q_len) or null
     void *out;
     int32_t out_bf16;
     float *lse;
     float *ws_acc, *ws_ml;
     uint32_t *status;
 };
+
+// Paged KV append (kv_append.cu).
+struct AppendParams {
+    const void *k_new, *v_new;  // [B][Hkv][max_new][D]
+    void *k_pages, *v_pages;    // [num_pages][Hkv][P][D]
+    const int32_t *page_table, *seq_lens, *n_new;
+    int32_t B, Hkv, max_new, P, max_pages, num_pages, row_bytes;
+    uint32_t *status;
+};
+cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t stream);
 
 cudaError_t launch_fmha_tc(const TcParams &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                            const CUtensorMap &tmV, cudaStream_t stream);

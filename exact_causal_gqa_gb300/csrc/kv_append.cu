@@ -1,0 +1,65 @@
+// kv_append.cu -- the write before the attention: the new tokens' K and V rows of
+// each sequence go to the page slots of positions seq_lens[b] .. seq_lens[b] +
+// n_new[b] - 1, found through the page table (CFR-Atlas README, "Minimal
+// integration": row-major K[token][dim] per (layer, kv head, token range);
+// ferrox-core "cache" module: a KV cache grown one position at a time).
+//
+// A grid-stride loop moves 16 bytes of K and 16 bytes of V per thread and step;
+// consecutive threads cover consecutive 16-byte pieces of a row, so both the
+// reads of the new rows and the writes into a page slot are coalesced.  Memory
+// bound: 2 x (read + write) x rows x head_dim x element size.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace atlas {
+namespace {
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+    const int vec = p.row_bytes / 16;  // 16-byte pieces per row
+    const int64_t total = (int64_t)p.B * p.Hkv * p.max_new * vec;
+    const char *kn = static_cast<const char *>(p.k_new);
+    const char *vn = static_cast<const char *>(p.v_new);
+    char *kp = static_cast<char *>(p.k_pages);
+    char *vp = static_cast<char *>(p.v_pages);
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int piece = (int)(idx % vec);
+        const int64_t row = idx / vec;  // (b, g, j)
+        const int j = (int)(row % p.max_new);
+        const int g = (int)((row / p.max_new) % p.Hkv);
+        const int b = (int)(row / ((int64_t)p.max_new * p.Hkv));
+        const int cnt = p.n_new ? p.n_new[b] : p.max_new;
+        if (cnt < 0 || cnt > p.max_new) {
+            if (j == 0 && g == 0 && piece == 0 && p.status) atomicOr(p.status, ATLAS_DEV_BAD_SEQLEN);
+            continue;
+        }
+        if (j >= cnt) continue;
+        const int64_t t = (int64_t)p.seq_lens[b] + j;
+        if (t < 0 || t >= (int64_t)p.max_pages * p.P) {
+            if (p.status && piece == 0) atomicOr(p.status, ATLAS_DEV_BAD_SEQLEN);
+            continue;
+        }
+        const int page = p.page_table[(int64_t)b * p.max_pages + t / p.P];
+        if (page < 0 || page >= p.num_pages) {
+            if (p.status && piece == 0) atomicOr(p.status, ATLAS_DEV_BAD_PAGE);
+            continue;
+        }
+        const int64_t src = row * p.row_bytes + piece * 16;
+        const int64_t dst = (((int64_t)page * p.Hkv + g) * p.P + t % p.P) * p.row_bytes + piece * 16;
+        *reinterpret_cast<uint4 *>(kp + dst) = *reinterpret_cast<const uint4 *>(kn + src);
+        *reinterpret_cast<uint4 *>(vp + dst) = *reinterpret_cast<const uint4 *>(vn + src);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t stream) {
+    const int64_t total = (int64_t)p.B * p.Hkv * p.max_new * (p.row_bytes / 16);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    kv_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace atlas

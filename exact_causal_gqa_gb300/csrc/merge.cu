@@ -26,13 +26,16 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) merge_kernel(const MergePara
     const int i = (int)(row % p.q_len);
     const int b = (int)(row / ((int64_t)p.Hq * p.q_len));
     const int L = p.seq_lens[b];
-    const bool bad_len = L < p.q_len || L > p.max_pages * p.P || (p.require_full && L != p.q_len);
+    const int qn = p.q_lens ? p.q_lens[b] : p.q_len;  // ragged: query rows of sequence b
+    const bool bad_len = qn < 0 || qn > p.q_len || L < qn || L > p.max_pages * p.P ||
+                         (p.require_full && L != qn);
+    if (!bad_len && i >= qn) return;  // padding row: not a query, not written
 
     float o[DPL];
     float lse = __int_as_float(0x7fc00000);
     bool nan_row = bad_len;
     if (!bad_len) {
-        const int visible = L - p.q_len + i + 1;
+        const int visible = L - qn + i + 1;
         // splits holding this row's keys: [first, nsplit)
         const int first = p.window > 0 ? max(0, visible - p.window) / p.chunk : 0;
         const int nsplit = (visible + p.chunk - 1) / p.chunk;

@@ -32,8 +32,10 @@ __device__ __forceinline__ void record(uint32_t *status, uint32_t bit) {
     if (status) atomicOr(status, bit);
 }
 
-__device__ __forceinline__ bool seq_len_bad(const SplitParams &p, int L) {
-    return L < p.q_len || L > p.max_pages * p.P || (p.require_full && L != p.q_len);
+// qn: the sequence's query rows (q_lens[b] when ragged, else q_len).
+__device__ __forceinline__ bool seq_len_bad(const SplitParams &p, int L, int qn) {
+    return qn < 0 || qn > p.q_len || L < qn || L > p.max_pages * p.P ||
+           (p.require_full && L != qn);
 }
 
 // Flat output row of column n of (b, hkv).
@@ -43,7 +45,9 @@ __device__ __forceinline__ int64_t column_row(const SplitParams &p, int b, int h
     return ((int64_t)b * p.Hq + h) * p.q_len + i;
 }
 
-// Keys visible to column n (absolute count), as defined by the suffix rule.
+// Keys visible to column n (absolute count), as defined by the suffix rule.  L
+// here is the sequence length shifted by q_len - qn (see split_prologue), so the
+// same formula serves ragged batches.
 __device__ __forceinline__ int column_visible(const SplitParams &p, int L, int n) {
     return L - p.q_len + (n % p.q_len) + 1;
 }
@@ -61,24 +65,32 @@ __device__ __forceinline__ float score_log2(const SplitParams &p, float raw) {
 
 // Shared prologue: decides whether this CTA has work.  Returns false when the
 // CTA must exit (nothing visible, or an error that has been recorded).
+// Returns L shifted to L - qn + q_len: with it, row i (< qn) of a ragged sequence
+// sits at position L_shifted - q_len + i = seq_len - qn + i, as in a full batch.
+// Columns with row index >= qn are padding (qn out).
 template <int NCOLS>
 __device__ bool split_prologue(const SplitParams &p, int &L, int &kv_begin, int &kv_end,
-                               int &col0, int &ncols) {
+                               int &col0, int &ncols, int &qn) {
     const int b = blockIdx.z;
     const int hkv = blockIdx.y / p.col_tiles;
     const int ct = blockIdx.y % p.col_tiles;
     L = p.seq_lens[b];
-    if (seq_len_bad(p, L)) {
+    qn = p.q_lens ? p.q_lens[b] : p.q_len;
+    if (seq_len_bad(p, L, qn)) {
         if (threadIdx.x == 0 && blockIdx.x == 0) record(p.status, ATLAS_DEV_BAD_SEQLEN);
         return false;  // the merge writes NaN rows for this sequence
     }
+    L = L - qn + p.q_len;
     col0 = ct * NCOLS;
     ncols = min(NCOLS, p.G * p.q_len - col0);
-    int i_max = 0, i_min = p.q_len;
+    int i_max = -1, i_min = p.q_len;
     for (int c = 0; c < ncols; ++c) {
-        i_max = max(i_max, (col0 + c) % p.q_len);
-        i_min = min(i_min, (col0 + c) % p.q_len);
+        const int i = (col0 + c) % p.q_len;
+        if (i >= qn) continue;  // padding row of a ragged batch
+        i_max = max(i_max, i);
+        i_min = min(i_min, i);
     }
+    if (i_max < 0) return false;  // only padding rows
     const int kv_hi = L - p.q_len + i_max + 1;
     // Keys below every column's window are skipped whole (64-key blocks).
     const int kv_lo = p.window > 0 ? max(0, L - p.q_len + i_min + 1 - p.window) : 0;
@@ -172,8 +184,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
     const uint32_t empty0 = full0 + STAGES * 8;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lay::kFlags);
 
-    int L, kv_begin, kv_end, col0, ncols;
-    if (!split_prologue<NCOLS>(p, L, kv_begin, kv_end, col0, ncols)) return;
+    int L, kv_begin, kv_end, col0, ncols, qn;
+    if (!split_prologue<NCOLS>(p, L, kv_begin, kv_end, col0, ncols, qn)) return;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int b = blockIdx.z;
@@ -278,8 +290,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int c = nt * 8 + 2 * (lane % 4) + e;
-                lim[nt][e] = c < ncols ? min(kv_end, column_visible(p, L, col0 + c)) : 0;
-                lo[nt][e] = c < ncols ? column_first(p, L, col0 + c) : 0;
+                const bool real = c < ncols && (col0 + c) % p.q_len < qn;
+                lim[nt][e] = real ? min(kv_end, column_visible(p, L, col0 + c)) : 0;
+                lo[nt][e] = real ? column_first(p, L, col0 + c) : 0;
                 m_run[nt][e] = -INFINITY;
                 l_run[nt][e] = 0.f;
             }
@@ -450,8 +463,8 @@ __global__ void __launch_bounds__(128)
     __shared__ float cm[W * NC], cl[W * NC];
     __shared__ float cacc[W * NC * D];
 
-    int L, kv_begin, kv_end, col0, ncols;
-    if (!split_prologue<NC>(p, L, kv_begin, kv_end, col0, ncols)) return;
+    int L, kv_begin, kv_end, col0, ncols, qn;
+    if (!split_prologue<NC>(p, L, kv_begin, kv_end, col0, ncols, qn)) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int b = blockIdx.z;
     const int hkv = blockIdx.y / p.col_tiles;
@@ -462,7 +475,7 @@ __global__ void __launch_bounds__(128)
     int lim[NC], lo[NC];
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        const bool ok = c < ncols;
+        const bool ok = c < ncols && (col0 + c) % p.q_len < qn;
         const float *qrow = ok ? static_cast<const float *>(p.q) +
                                      column_row(p, b, hkv, col0 + c) * D
                                : nullptr;

@@ -120,6 +120,13 @@ typedef struct {
     const float *sinks;        /* optional device [n_q_heads]: a logit per q head that joins
                                   the softmax denominator (natural-log units, like the
                                   scaled scores) with no value row; lse includes it */
+    const int32_t *q_lens;     /* optional device [batch]: ragged query counts (chunked
+                                  prefill).  Sequence b has q_lens[b] <= q_len query rows,
+                                  the last q_lens[b] positions of its K/V: row i sits at
+                                  seq_lens[b] - q_lens[b] + i.  Rows i >= q_lens[b] of q
+                                  are ignored and of out / lse are not written.  NULL:
+                                  every sequence has q_len rows.  Prefill then needs
+                                  seq_lens[b] == q_lens[b]. */
 } atlas_launch;
 
 /*
@@ -161,6 +168,37 @@ atlas_status atlas_attn_prefill(const void *q, const void *k_pages, const void *
  */
 size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,
                                  int32_t head_dim, int32_t page_tokens, const atlas_launch *L);
+
+/* Arguments of atlas_kv_append beyond its pointer / size list. */
+typedef struct {
+    int32_t batch;
+    int32_t max_pages_per_seq;
+    int32_t num_pages;
+    int32_t max_new;           /* rows per sequence in k_new / v_new */
+    atlas_dtype kv_dtype;      /* element type of k_new, v_new and the pools */
+    uint32_t *status_word;     /* optional device word (ATLAS_DEV_* bits) */
+    void *stream;              /* cudaStream_t; NULL = the legacy default stream */
+} atlas_append;
+
+/*
+ * atlas_kv_append: the write before attention -- the paged KV cache grown by the
+ * new tokens of each sequence (ferrox-core "cache" module: a KV cache growable one
+ * position at a time; CFR-Atlas README, "Minimal integration": row-major
+ * K[token][dim] per (layer, kv head, token range)).  For b < batch, kv head g and
+ * j < n_new[b] (n_new NULL: all max_new rows):
+ *   k_pages[page_table[b][t / page_tokens]][g][t % page_tokens][:] = k_new[b][g][j][:]
+ *   (and v), with t = seq_lens[b] + j.
+ * k_new, v_new: device [batch][n_kv_heads][max_new][head_dim], read only; the pools
+ * are written in place; seq_lens (the lengths BEFORE the append) and n_new are
+ * device int32 [batch], read only -- the caller advances seq_lens itself.  The
+ * pages for the new positions must already be in page_table.  A page id outside
+ * [0, num_pages) or a position past max_pages_per_seq * page_tokens sets
+ * ATLAS_DEV_BAD_PAGE / ATLAS_DEV_BAD_SEQLEN and that row is skipped.
+ */
+atlas_status atlas_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
+                             const int32_t *page_table, const int32_t *seq_lens,
+                             const int32_t *n_new, int32_t n_kv_heads, int32_t head_dim,
+                             int32_t page_tokens, const atlas_append *A);
 
 /* Static, human-readable text for a status code. */
 const char *atlas_attn_status_string(atlas_status status);
