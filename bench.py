@@ -53,6 +53,10 @@ def parse_args():
     ap.add_argument("--window", type=int, default=0, help="sliding window (keys); 0 = none")
     ap.add_argument("--softcap", type=float, default=0.0, help="logit softcap; 0 = none")
     ap.add_argument("--sinks", action="store_true", help="one sink logit per q head")
+    ap.add_argument("--ragged", action="store_true",
+                    help="ragged query counts: q_lens[b] ~ U{1..q_len} (suffix/prefill)")
+    ap.add_argument("--append", action="store_true",
+                    help="time atlas_kv_append writing the workload's K/V into its pages")
     return ap.parse_args()
 
 
@@ -88,6 +92,15 @@ def peaks():
             data = json.load(f)
         return data, "measured"
     return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+def work_of_ragged(prob, q_lens):
+    """(KV bytes, FLOPs) with q_lens[b] query rows per sequence (no window)."""
+    lens = prob.seq_lens.to(torch.int64).cpu()
+    qn = q_lens.to(torch.int64).cpu()
+    keys = int((qn * (lens - qn) + qn * (qn + 1) // 2).sum())
+    kv = 2 * int(lens.sum()) * prob.n_kv_heads * prob.head_dim * prob.k_pages.element_size()
+    return kv, 4 * prob.head_dim * prob.n_q_heads * keys
 
 
 def work_of(prob, window: int = 0):
@@ -211,6 +224,13 @@ def run_atlas(args, world, rank, local):
     prob = inputs.make_config(args.config, seed=seed, device=dev, **overrides)
     kv_bytes, flops = work_of(prob, args.window)
     variants = dict(window=args.window, softcap=args.softcap)
+    if args.ragged:
+        g = torch.Generator().manual_seed(seed + 7)
+        q_lens = torch.randint(1, prob.q_len + 1, (prob.batch,), generator=g, dtype=torch.int32)
+        if prob.kind == "prefill":  # a ragged prompt batch: each prompt is its own length
+            prob.seq_lens = q_lens.to(dev)
+        variants["q_lens"] = q_lens.to(dev)
+        kv_bytes, flops = work_of_ragged(prob, q_lens)
     if args.sinks:
         g = torch.Generator().manual_seed(seed)
         variants["sinks"] = (torch.randn(prob.n_q_heads, generator=g) * 2.0).float().to(dev)
@@ -343,7 +363,8 @@ def run_atlas(args, world, rank, local):
         "config": {
             "workload": cfg["name"] + (f" (batch {args.batch})" if args.batch else "") +
             (f" window {args.window}" if args.window else "") +
-            (f" softcap {args.softcap}" if args.softcap else "") + (" sinks" if args.sinks else ""),
+            (f" softcap {args.softcap}" if args.softcap else "") + (" sinks" if args.sinks else "") +
+            (" ragged" if args.ragged else ""),
             "kind": prob.kind, "batch": prob.batch, "n_q_heads": prob.n_q_heads,
             "n_kv_heads": prob.n_kv_heads, "head_dim": prob.head_dim,
             "page_tokens": prob.page_tokens, "q_len": prob.q_len,
@@ -389,6 +410,57 @@ def run_atlas(args, world, rank, local):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config, prob, decode_like)
     return line
+
+
+def run_append(args, world, rank, local):
+    """Time atlas_kv_append writing every token of the workload's K/V into its pages
+    (as a prefill would): bytes = read + write of K and V rows."""
+    import exact_causal_gqa_gb300 as atlas
+    from exact_causal_gqa_gb300 import inputs
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = inputs.CONFIGS[args.config]
+    overrides = {"B": args.batch} if args.batch else {}
+    prob = inputs.make_config(args.config, seed=rank_seed(args.config, rank), device=dev,
+                              **overrides)
+    lens = prob.seq_lens.to(torch.int64)
+    max_new = int(lens.max())
+    g = torch.Generator(device=dev).manual_seed(5)
+    k_new = torch.randn((prob.batch, prob.n_kv_heads, max_new, prob.head_dim), generator=g,
+                        device=dev).to(prob.k_pages.dtype)
+    v_new = torch.randn_like(k_new)
+    zeros = torch.zeros(prob.batch, dtype=torch.int32, device=dev)
+    moved = 2 * 2 * int(lens.sum()) * prob.n_kv_heads * prob.head_dim * prob.k_pages.element_size()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        atlas.kv_append(k_new, v_new, prob.k_pages, prob.v_pages, prob.page_table, zeros,
+                        prob.seq_lens, status=status)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    gbs = job_rate(moved, world, ms, 1e9)
+    peak = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
+    return {"metric": "KV append GB/s (read + write)", "value": round(gbs, 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": prob.dtype, "data": "synthetic",
+            "config": {"workload": cfg["name"] + " (append all tokens)", "bytes_moved": moved},
+            "roofline": {"kernel": "kv_append_kernel", "bound": "hbm", "achieved": round(gbs, 3),
+                         "peak": peak, "peak_source": pk_kind, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None},
+            "gpu_launches": args.steps, "device_status": int(status.item())}
 
 
 def oracle_sample(index, prob_host, decode_like, budget_s):
@@ -485,7 +557,7 @@ def main():
     else:
         if world > 1:
             torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-        line = run_atlas(args, world, rank, local)
+        line = (run_append if args.append else run_atlas)(args, world, rank, local)
         if world > 1:
             torch.distributed.destroy_process_group()
     if line is not None:

@@ -474,7 +474,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const uint32_t ts = tl + C::s_col(x, bsel);
             const int nvis = lim_row - (kv_begin + j * BN);  // visible columns: [nlo, nvis)
             const int nlo = lo_row - (kv_begin + j * BN);
-            const bool all_visible = __all_sync(0xffffffffu, nvis >= BN && nlo <= 0);
+            // Padding rows of a ragged batch never reach the output: they may take the
+            // unmasked path (their O and l are garbage but stay in their own row).
+            const bool all_visible = __all_sync(0xffffffffu, !valid || (nvis >= BN && nlo <= 0));
             // Pass 1: row max of the raw scores (scale_log2 >= 0, so the scaled
             // maximum is the maximum scaled), four chains of 3-input max.
             // Outer loops stay rolled: a fully unrolled body overflows the
@@ -509,7 +511,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     }
                 }
             }
-            const float mraw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            // (a padding row keeps m = -inf: it never asks for an O rescale)
+            const float mraw = valid ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) : -INFINITY;
             // the softcap is increasing, so it maps the raw maximum to the maximum
             const float mx = mraw == -INFINITY ? -INFINITY
                              : capped ? p.softcap_log2 * tanh_acc(mraw * p.softcap_inv)
