@@ -335,29 +335,35 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             constexpr uint32_t idPV = idesc_bf16_f32(128, 128, true);
             bool ok = mbar_wait_bounded(BAR(C::B_Q), 0, abort_flag, kWaitLimitNs);
             tc_fence_after();
-            // S_x(j) = Q_x K_j^T for every tile into S buffer j % SB.
-            auto issue_s = [&](int j) -> bool {
+            // S_x(j) = Q_x K_j^T into S buffer j % SB of tile x.  Tile 0 waits for
+            // K_j; the last tile releases its stage.
+            auto issue_s = [&](int j, int x) -> bool {
                 const int s = j % S;
-                if (!mbar_wait_bounded(BAR(C::B_KFULL + s), (j / S) & 1, abort_flag, kWaitLimitNs))
-                    return false;
-                tc_fence_after();
-                const uint32_t kbase = sb + C::OFF_K + s * kTileBytes;
-#pragma unroll
-                for (int x = 0; x < NT; ++x) {
-                    const uint32_t qbase = sb + C::OFF_Q + x * kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-                        umma_bf16(tmem + C::s_col(x, j % SB), sdesc_sw128(qbase + off, 16, 1024),
-                                  sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0);
-                    }
-                    umma_commit(BAR(C::B_SFULL + x * SB + j % SB));
+                if (x == 0) {
+                    if (!mbar_wait_bounded(BAR(C::B_KFULL + s), (j / S) & 1, abort_flag,
+                                           kWaitLimitNs))
+                        return false;
+                    tc_fence_after();
                 }
-                umma_commit(BAR(C::B_KEMPTY + s));
-                TRACE(1, 1, j);
+                const uint32_t kbase = sb + C::OFF_K + s * kTileBytes;
+                const uint32_t qbase = sb + C::OFF_Q + x * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
+                    umma_bf16(tmem + C::s_col(x, j % SB), sdesc_sw128(qbase + off, 16, 1024),
+                              sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0);
+                }
+                umma_commit(BAR(C::B_SFULL + x * SB + j % SB));
+                if (x == NT - 1) {
+                    umma_commit(BAR(C::B_KEMPTY + s));
+                    TRACE(1, 1, j);
+                }
                 return true;
             };
-            for (int j = 0; ok && j < min(SB, nb); ++j) ok = issue_s(j);
+            for (int j = 0; ok && j < min(SB, nb); ++j)
+#pragma unroll
+                for (int x = 0; x < NT; ++x)
+                    if (ok) ok = issue_s(j, x);
             for (int j = 0; ok && j < nb; ++j) {
                 const int s = j % S;
 #pragma unroll
@@ -403,20 +409,18 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     }
                     umma_commit(BAR(C::B_PVDONE + x));
                     TRACE(1, 4 + 16 * x, j);
+                    // Ping-pong: S_x(j + SB) follows PV_x(j) at once, so tile x starts
+                    // its next softmax while the other tile's P is still being made.
+                    // It writes the S buffer that PV_x(j) reads P_x(j) from; the
+                    // tcgen05.mma operations of one thread run in issue order, so
+                    // PV_x(j) has read its operand before S_x(j + SB) writes there.
+                    if (j + SB < nb && !issue_s(j + SB, x)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 if (!ok) break;
                 umma_commit(BAR(C::B_VEMPTY + s));
-                const int jn = j + SB;
-                if (jn < nb) {
-                    // S buffer jn % SB holds P_x(j) until PV_x(j) has run.
-#pragma unroll
-                    for (int x = 0; x < NT; ++x)
-                        if (ok && !mbar_wait_bounded(BAR(C::B_PVDONE + x), j & 1, abort_flag,
-                                                     kWaitLimitNs))
-                            ok = false;
-                    TRACE(1, 5, j);
-                    if (ok) ok = issue_s(jn);
-                }
             }
             if (!ok) {
                 failed = true;
@@ -597,8 +601,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             if (r == 0) TRACE(2 + x, 6, j + 0 * (int)(l != l));
             // O must hold PV(j-1) before it is rescaled (and before PV(j) is issued,
             // which waits for this warpgroup's P).  Doing it after writing P keeps
-            // PV(j-1) off the critical path.  With one S buffer the MMA issued S(j)
-            // only after PV(j-1) completed, so S being full already says so.
+            // PV(j-1) off the critical path.  With one S buffer S(j) was issued after
+            // PV(j-1) by the same thread, and its commit tracks every earlier MMA, so
+            // S being full already says so.
             if (SB > 1 && j > 0 && !wait_warp(BAR(C::B_PVDONE + x), (j - 1) & 1, abort_flag)) {
                 ok = false;
                 break;
