@@ -58,7 +58,32 @@ class _Launch(ctypes.Structure):
                 ("stream", ctypes.c_void_p), ("split_tokens", ctypes.c_int32),
                 ("debug_flags", ctypes.c_uint32), ("events", ctypes.c_void_p),
                 ("window", ctypes.c_int32), ("softcap", ctypes.c_float),
-                ("sinks", ctypes.c_void_p), ("q_lens", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("q_lens", ctypes.c_void_p),
+                ("chunk_range", ctypes.c_void_p), ("phase", ctypes.c_int32)]
+
+PHASE_ALL, PHASE_CHUNKS, PHASE_MERGE = 0, 1, 2
+
+
+class _PoolConfig(ctypes.Structure):
+    _fields_ = [("hot_slots", ctypes.c_int32), ("scratch_slots", ctypes.c_int32),
+                ("page_tokens", ctypes.c_int32), ("host_pages", ctypes.c_int32)]
+
+
+class _PoolRequest(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+                ("host_page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("chunk_tokens", ctypes.c_int32), ("keep_recent_tokens", ctypes.c_int32),
+                ("admit", ctypes.c_int32)]
+
+
+class PoolStats(ctypes.Structure):
+    """What one plan of a HotPagePool did (atlas_pool_stats)."""
+    _fields_ = [("passes", ctypes.c_int32), ("pages", ctypes.c_int64), ("hits", ctypes.c_int64),
+                ("admitted", ctypes.c_int64), ("evicted", ctypes.c_int64),
+                ("scratch_loads", ctypes.c_int64), ("copies", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class _Append(ctypes.Structure):
@@ -100,6 +125,27 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.atlas_kv_append.restype = ctypes.c_int
     lib.atlas_attn_status_string.argtypes = [ctypes.c_int]
     lib.atlas_attn_status_string.restype = ctypes.c_char_p
+    lib.atlas_attn_split_tokens.argtypes = [ctypes.c_int] + [ctypes.c_int32] * 4 + [
+        ctypes.POINTER(_Launch)]
+    lib.atlas_attn_split_tokens.restype = ctypes.c_int32
+    lib.atlas_pool_create.argtypes = [ctypes.POINTER(_PoolConfig), ctypes.POINTER(ctypes.c_void_p)]
+    lib.atlas_pool_create.restype = ctypes.c_int
+    lib.atlas_pool_destroy.argtypes = [ctypes.c_void_p]
+    lib.atlas_pool_destroy.restype = None
+    lib.atlas_pool_plan.argtypes = [ctypes.c_void_p, ctypes.POINTER(_PoolRequest),
+                                    ctypes.POINTER(PoolStats)]
+    lib.atlas_pool_plan.restype = ctypes.c_int
+    lib.atlas_pool_pass.argtypes = [ctypes.c_void_p, ctypes.c_int32] + [ctypes.c_void_p] * 3 + [
+        ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+    lib.atlas_pool_pass.restype = ctypes.c_int
+    lib.atlas_pool_slot_of.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    lib.atlas_pool_slot_of.restype = ctypes.c_int32
+    lib.atlas_pool_invalidate.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    lib.atlas_pool_invalidate.restype = None
+    lib.atlas_pool_fill.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int32, ctypes.c_int64,
+                                                            ctypes.c_int32, ctypes.c_int32,
+                                                            ctypes.c_void_p, ctypes.c_void_p]
+    lib.atlas_pool_fill.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -114,7 +160,8 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=None,
             status=None, stream=None, split_tokens=0, debug_flags=0, events=None,
-            window=0, softcap=0.0, sinks=None, q_lens=None) -> _Launch:
+            window=0, softcap=0.0, sinks=None, q_lens=None, chunk_range=None,
+            phase=PHASE_ALL) -> _Launch:
     L = _Launch()
     L.batch, L.q_len = q.shape[0], q.shape[2]
     L.max_pages_per_seq = page_table.shape[1]
@@ -135,15 +182,17 @@ def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=Non
     L.softcap = softcap
     L.sinks = _ptr(sinks)
     L.q_lens = _ptr(q_lens)
+    L.chunk_range = _ptr(chunk_range)
+    L.phase = phase
     return L
 
 
 def workspace_size(kind: str, q_shape, n_q_heads, n_kv_heads, head_dim, page_tokens,
                    max_pages_per_seq, num_pages, dtype=torch.bfloat16,
-                   out_dtype=None, split_tokens=0, window=0) -> int:
-    """Workspace bytes a call needs (from shapes, split size and window only)."""
+                   out_dtype=None, split_tokens=0, window=0, phase=PHASE_ALL) -> int:
+    """Workspace bytes a call needs (from shapes, split size, window and phase only)."""
     L = _Launch()
-    L.window = window
+    L.window, L.phase = window, phase
     L.batch, L.q_len = q_shape[0], q_shape[2]
     L.max_pages_per_seq, L.num_pages = max_pages_per_seq, num_pages
     L.q_dtype = L.kv_dtype = _DTYPES.get(dtype, -1)
@@ -159,12 +208,15 @@ def workspace_size(kind: str, q_shape, n_q_heads, n_kv_heads, head_dim, page_tok
 def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads,
           head_dim, page_tokens, scale, *, out=None, out_dtype=None, lse=None,
           workspace=None, status=None, split_tokens=0, debug_flags=0, events=None,
-          window=0, softcap=0.0, sinks=None, q_lens=None):
+          window=0, softcap=0.0, sinks=None, q_lens=None, chunk_range=None,
+          phase=PHASE_ALL):
     """``events``: optional ctypes array of three cudaEvent_t handles (see
     EventTimer) recorded around the main kernel and the merge.  ``window``,
     ``softcap`` and ``sinks`` (float32 CUDA tensor [n_q_heads]) select the score /
     mask variants; the defaults give plain causal attention.  ``q_lens`` (int32
-    CUDA tensor [B]) makes the batch ragged: sequence b has q_lens[b] query rows."""
+    CUDA tensor [B]) makes the batch ragged: sequence b has q_lens[b] query rows.
+    ``phase`` and ``chunk_range`` (int32 CUDA tensor [B][2]) spread one call over
+    several launches sharing ``workspace`` (atlas_launch.phase)."""
     lib = load_library()
     for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
                     ("page_table", page_table), ("seq_lens", seq_lens)):
@@ -175,8 +227,12 @@ def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_
     if q.dim() != 4 or k_pages.dim() != 4 or v_pages.shape != k_pages.shape:
         raise ValueError("q must be [B][Hq][q_len][D] and pools [num_pages][Hkv][P][D]")
     out_dtype = out_dtype or (out.dtype if out is not None else q.dtype)
-    if out is None:
+    if out is None and phase != PHASE_CHUNKS:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if chunk_range is not None and (not chunk_range.is_cuda or chunk_range.dtype != torch.int32
+                                    or chunk_range.numel() != 2 * q.shape[0]
+                                    or not chunk_range.is_contiguous()):
+        raise ValueError("chunk_range must be a contiguous int32 CUDA tensor [batch][2]")
     if status is not None and (status.dtype != torch.int32 or status.numel() < 1):
         raise ValueError("status must be an int32 device tensor")
     if sinks is not None and (not sinks.is_cuda or sinks.dtype != torch.float32 or
@@ -189,7 +245,7 @@ def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_
     L = _launch(q, k_pages, page_table, out_dtype, out, lse, None, status, stream,
                 split_tokens, debug_flags,
                 None if events is None else ctypes.cast(events, ctypes.c_void_p).value,
-                window, softcap, sinks, q_lens)
+                window, softcap, sinks, q_lens, chunk_range, phase)
     need = lib.atlas_attn_workspace_size(_KINDS[kind], n_q_heads, n_kv_heads, head_dim,
                                          page_tokens, ctypes.byref(L))
     if workspace is None and 0 < need < ctypes.c_size_t(-1).value:
@@ -203,6 +259,24 @@ def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_
     if rc != 0:
         raise AtlasError(rc, status_string(rc))
     return out
+
+
+def split_tokens_of(kind: str, q_shape, n_q_heads, n_kv_heads, head_dim, page_tokens,
+                    max_pages_per_seq, num_pages, dtype=torch.bfloat16, out_dtype=None,
+                    split_tokens=0, window=0, phase=PHASE_ALL) -> int:
+    """Keys per split-KV chunk of such a call (0: no chunks), atlas_attn_split_tokens."""
+    L = _Launch()
+    L.window, L.phase = window, phase
+    L.batch, L.q_len = q_shape[0], q_shape[2]
+    L.max_pages_per_seq, L.num_pages = max_pages_per_seq, num_pages
+    L.q_dtype = L.kv_dtype = _DTYPES.get(dtype, -1)
+    L.out_dtype = _DTYPES.get(out_dtype or dtype, -1)
+    L.split_tokens = split_tokens
+    n = load_library().atlas_attn_split_tokens(_KINDS[kind], n_q_heads, n_kv_heads, head_dim,
+                                               page_tokens, ctypes.byref(L))
+    if n < 0:
+        raise AtlasError(1, "invalid arguments for split_tokens_of")
+    return n
 
 
 def decode(q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_heads, head_dim,
@@ -293,3 +367,6 @@ def run_host(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_
     host_out.copy_(out, non_blocking=True)
     torch.cuda.current_stream(out.device).synchronize()
     return host_out
+
+
+from .pool import HotPagePool  # noqa: E402  (the pool binding uses the names above)

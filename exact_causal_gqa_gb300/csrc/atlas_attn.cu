@@ -98,6 +98,9 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     if (L->q_len > max_ctx) return ATLAS_ERR_INVALID_ARG;
     if (L->split_tokens < 0 || L->split_tokens % kSplitBlockTokens != 0)
         return ATLAS_ERR_INVALID_ARG;
+    if (L->phase != ATLAS_PHASE_ALL && L->phase != ATLAS_PHASE_CHUNKS &&
+        L->phase != ATLAS_PHASE_MERGE)
+        return ATLAS_ERR_INVALID_ARG;
 
     const int G = Hq / Hkv;
     plan->G = G;
@@ -114,7 +117,8 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         int64_t chunk = 0;
         if (L->split_tokens > 0) {
             chunk = round_up(L->split_tokens, 128);
-        } else if (tiles < kTcDirectTiles && !(L->debug_flags & ATLAS_DEBUG_TC_DIRECT)) {
+        } else if ((tiles < kTcDirectTiles || L->phase != ATLAS_PHASE_ALL) &&
+                   !(L->debug_flags & ATLAS_DEBUG_TC_DIRECT)) {
             chunk = round_up((work_ctx * tiles + kTcPlanCtas - 1) / kTcPlanCtas, 128);
             if (chunk < 1024) chunk = 1024;
             if (chunk > 8192) chunk = 8192;
@@ -130,7 +134,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
             plan->ml_offset = (size_t)round_up((int64_t)plan->acc_bytes, 256);
             plan->ws_bytes = plan->ml_offset + (size_t)rows * plan->n_chunks * 2 * sizeof(float);
         } else {
-            if (tiles > INT32_MAX) return ATLAS_ERR_UNSUPPORTED;
+            if (tiles > INT32_MAX || L->phase != ATLAS_PHASE_ALL) return ATLAS_ERR_UNSUPPORTED;
             plan->chunk = plan->n_chunks = 0;
             plan->tiles_per_head = (L->q_len % 128 == 0) ? L->q_len / 128 : 0;
             plan->acc_bytes = plan->ml_offset = plan->ws_bytes = 0;
@@ -199,7 +203,8 @@ atlas_status encode_pool_map(CUtensorMap *map, const void *pool, int32_t num_pag
 atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void *v_pages,
                  const int32_t *page_table, const int32_t *seq_lens, int32_t Hq, int32_t Hkv,
                  int32_t D, int32_t P, float scale, const atlas_launch *L) {
-    if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !L || !L->out)
+    if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !L ||
+        (!L->out && L->phase != ATLAS_PHASE_CHUNKS))
         return ATLAS_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(L->out) ||
         !aligned16(L->workspace))
@@ -240,6 +245,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     sp.scale_log2 = scale * kLog2e;
     sp.window = L->window;
     sp.q_lens = L->q_lens;
+    sp.chunk_range = L->chunk_range;
     sp.softcap_log2 = L->softcap > 0.f ? L->softcap * kLog2e : 0.f;
     sp.softcap_inv = L->softcap > 0.f ? scale / L->softcap : 0.f;
     sp.ws_acc = static_cast<float *>(L->workspace);
@@ -251,7 +257,10 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     if (L->events)
         for (int i = 0; i < 3; ++i) ev[i] = static_cast<cudaEvent_t>(L->events[i]);
     cudaError_t err;
-    if (plan.path == Path::TensorCore) {
+    if (L->phase == ATLAS_PHASE_MERGE) {
+        if (ev[0] && cudaEventRecord(ev[0], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+        if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+    } else if (plan.path == Path::TensorCore) {
         CUtensorMap tmQ, tmK, tmV;
         const int box = P < 128 ? P : 128;
         st = encode_rows_map(&tmQ, q, (int64_t)L->batch * Hq * L->q_len, D, 128);
@@ -285,6 +294,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         tp.softcap_inv = L->softcap > 0.f ? fabsf(scale) / L->softcap : 0.f;
         tp.sinks = L->sinks;
         tp.q_lens = L->q_lens;
+        tp.chunk_range = L->chunk_range;
         tp.out = L->out;
         tp.out_bf16 = L->out_dtype == ATLAS_BF16;
         tp.lse = L->lse;
@@ -312,6 +322,10 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     }
     if (err != cudaSuccess) return ATLAS_ERR_CUDA;
     if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+    }
+    if (L->phase == ATLAS_PHASE_CHUNKS) {
+        if (ev[2] && cudaEventRecord(ev[2], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
+        return ATLAS_OK;
     }
 
     MergeParams mp{};
@@ -413,6 +427,14 @@ size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_k
     if (atlas::make_plan(kind, n_q_heads, n_kv_heads, head_dim, page_tokens, L, &plan) != ATLAS_OK)
         return SIZE_MAX;
     return plan.ws_bytes;
+}
+
+int32_t atlas_attn_split_tokens(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,
+                                int32_t head_dim, int32_t page_tokens, const atlas_launch *L) {
+    atlas::Plan plan;
+    if (atlas::make_plan(kind, n_q_heads, n_kv_heads, head_dim, page_tokens, L, &plan) != ATLAS_OK)
+        return -1;
+    return plan.n_chunks > 0 ? plan.chunk : 0;
 }
 
 const char *atlas_attn_status_string(atlas_status status) {

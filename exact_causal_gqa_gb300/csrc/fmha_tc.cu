@@ -174,6 +174,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         }
     }
     const int b = u / p.Hkv, hkv = u % p.Hkv;
+    // A pass of a call spread over several launches computes some splits only.
+    if (p.split && p.chunk_range && (c < p.chunk_range[2 * b] || c >= p.chunk_range[2 * b + 1]))
+        return;
     const int seq_len = p.seq_lens[b];
     const int qn = p.q_lens ? p.q_lens[b] : p.q_len;  // query rows of this sequence
     const int rows_unit = p.G * p.q_len;

@@ -37,6 +37,7 @@ struct SplitParams {
     float softcap_log2;         // > 0: s2 = softcap_log2 * tanh(raw * softcap_inv)
     float softcap_inv;          // scale / softcap
     const int32_t *q_lens;      // [B] ragged query rows (<= q_len) or null
+    const int32_t *chunk_range; // [B][2] splits [lo, hi) this launch computes, or null (all)
     float *ws_acc;              // [B*Hq*q_len][n_chunks][D]   unnormalised accumulators
     float *ws_ml;               // [B*Hq*q_len][n_chunks][2]   (m in log2 units, l)
     uint32_t *status;           // may be null
@@ -77,6 +78,7 @@ struct TcParams {
     float softcap_inv;        // |scale| / softcap
     const float *sinks;       // [Hq] or null (direct mode folds it into the epilogue)
     const int32_t *q_lens;    // [B] ragged query rows (<= q_len) or null
+    const int32_t *chunk_range;  // split mode: [B][2] splits [lo, hi) to compute, or null
     void *out;
     int32_t out_bf16;
     float *lse;

@@ -74,6 +74,10 @@ __device__ bool split_prologue(const SplitParams &p, int &L, int &kv_begin, int 
     const int b = blockIdx.z;
     const int hkv = blockIdx.y / p.col_tiles;
     const int ct = blockIdx.y % p.col_tiles;
+    // A pass of a call spread over several launches computes some splits only.
+    if (p.chunk_range &&
+        ((int)blockIdx.x < p.chunk_range[2 * b] || (int)blockIdx.x >= p.chunk_range[2 * b + 1]))
+        return false;
     L = p.seq_lens[b];
     qn = p.q_lens ? p.q_lens[b] : p.q_len;
     if (seq_len_bad(p, L, qn)) {

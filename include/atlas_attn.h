@@ -127,7 +127,26 @@ typedef struct {
                                   are ignored and of out / lse are not written.  NULL:
                                   every sequence has q_len rows.  Prefill then needs
                                   seq_lens[b] == q_lens[b]. */
+    /* One call computed over several launches (the bounded hot-page pool of
+     * atlas_pool.h serves a context larger than its device slots this way): the
+     * split-KV chunks go to the same workspace pass by pass, then one merge reads
+     * them all.  Each chunk's partial state depends only on its keys, so the
+     * result is bit-identical to a single launch with the same sizes. */
+    const int32_t *chunk_range; /* optional device [batch][2]: compute only chunks s with
+                                   chunk_range[b][0] <= s < chunk_range[b][1] of sequence b
+                                   (chunks of atlas_attn_split_tokens keys, from key 0);
+                                   NULL = every chunk.  Only page_table entries of those
+                                   chunks' pages are read. */
+    int32_t phase;             /* ATLAS_PHASE_ALL, _CHUNKS or _MERGE (below) */
 } atlas_launch;
+
+/* atlas_launch.phase.  With a phase other than ALL the call always takes the
+ * split-KV form (the tensor-core path never writes its output directly). */
+#define ATLAS_PHASE_ALL 0    /* chunks, then the merge into out / lse */
+#define ATLAS_PHASE_CHUNKS 1 /* chunks only: partial states to the workspace */
+#define ATLAS_PHASE_MERGE 2  /* merge only: every chunk must have been computed by
+                                earlier ATLAS_PHASE_CHUNKS launches of the same sizes
+                                into this workspace, on this stream */
 
 /*
  * atlas_attn_decode: one query row per sequence (L->q_len must be 1), the
@@ -168,6 +187,16 @@ atlas_status atlas_attn_prefill(const void *q, const void *k_pages, const void *
  */
 size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,
                                  int32_t head_dim, int32_t page_tokens, const atlas_launch *L);
+
+/*
+ * Keys per split-KV chunk of the call of `kind` with these arguments (the
+ * chunks atlas_launch.chunk_range counts), 0 when the call has no chunks (the
+ * tensor-core path writing its output directly; never with a phase other than
+ * ATLAS_PHASE_ALL), -1 if the arguments are invalid.  Reads the same fields as
+ * atlas_attn_workspace_size.
+ */
+int32_t atlas_attn_split_tokens(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,
+                                int32_t head_dim, int32_t page_tokens, const atlas_launch *L);
 
 /* Arguments of atlas_kv_append beyond its pointer / size list. */
 typedef struct {
