@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--sinks", action="store_true", help="one sink logit per q head")
     ap.add_argument("--ragged", action="store_true",
                     help="ragged query counts: q_lens[b] ~ U{1..q_len} (suffix/prefill)")
+    ap.add_argument("--dtype", choices=["bf16", "f32"], default=None,
+                    help="override the config's q/K/V (and output) dtype")
     ap.add_argument("--pool", type=float, default=0.0,
                     help="serve the decode from a bounded hot-page pool holding this "
                          "fraction of the workload's pages (host tier in pinned memory)")
@@ -130,7 +132,9 @@ def work_of(prob, window: int = 0):
     return kv, flops
 
 
+F32_TILE_MIN_COLS = 64  # fp32 calls with this many columns per kv head take the tile kernel
 KERNEL_SOURCES = {"split_bf16_kernel": "split_kv.cu", "split_f32_kernel": "split_kv.cu",
+                  "split_f32_tile_kernel": "split_kv.cu",
                   "fmha_tc_kernel": "fmha_tc.cu"}
 
 
@@ -228,6 +232,8 @@ def run_atlas(args, world, rank, local):
     cfg = inputs.CONFIGS[args.config]
     seed = rank_seed(args.config, rank)
     overrides = {"B": args.batch} if args.batch else {}
+    if args.dtype:
+        overrides.update(dtype=args.dtype, out_dtype=args.dtype)
     prob = inputs.make_config(args.config, seed=seed, device=dev, **overrides)
     kv_bytes, flops = work_of(prob, args.window)
     variants = dict(window=args.window, softcap=args.softcap)
@@ -346,14 +352,27 @@ def run_atlas(args, world, rank, local):
         bound = "tensor"
     tc_path = prob.dtype == "bf16" and prob.head_dim == 128 and \
         prob.q_len * (prob.n_q_heads // prob.n_kv_heads) > 16
+    f32_tile = prob.dtype == "f32" and \
+        prob.q_len * (prob.n_q_heads // prob.n_kv_heads) >= F32_TILE_MIN_COLS
     if tc_path:
         kernel = "fmha_tc_kernel"
+    elif f32_tile:
+        kernel = "split_f32_tile_kernel"
     else:
         kernel = "split_bf16_kernel" if prob.dtype == "bf16" else "split_f32_kernel"
     # launches per step: the main kernel, plus the merge unless the tensor-core
     # path wrote the output directly (timer event 2 then coincides with event 1)
     merge_ms = sum(t.merge_ms() for t in timers) / len(timers)
     launches_per_step = 1 if (tc_path and ws_bytes == 0) else 2  # no workspace: no merge
+    if f32_tile:
+        # many-row fp32 work runs on the FFMA pipe: 152 SMs x 128 FMA / clock x 2
+        # flops at the SM clock sampled under load (nominal max 2070 MHz if none)
+        clk_now = clocks.summary(t_begin, t_end + 0.05) or \
+            clocks.summary(t_begin - 0.5, t_end + 0.05)
+        mhz = clk_now["sm_mhz"] if clk_now else 2070.0
+        peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
+        achieved = flops / (main_avg * 1e-3) / 1e12
+        bound, pk_kind = "alu", f"FFMA pipe: 152 SMs x 128 FMA/clk x 2 x {mhz:.0f} MHz"
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -369,6 +388,7 @@ def run_atlas(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
         "config": {
             "workload": cfg["name"] + (f" (batch {args.batch})" if args.batch else "") +
+            (f" as {args.dtype}" if args.dtype and args.dtype != cfg["dtype"] else "") +
             (f" window {args.window}" if args.window else "") +
             (f" softcap {args.softcap}" if args.softcap else "") + (" sinks" if args.sinks else "") +
             (" ragged" if args.ragged else ""),
@@ -394,7 +414,7 @@ def run_atlas(args, world, rank, local):
             "achieved": round(achieved, 3),
             "peak": peak,
             "peak_source": pk_kind,
-            "unit": unit,
+            "unit": "TFLOP/s" if f32_tile else unit,
             "frac": round(achieved / peak, 4),
             "traffic": traffic_record(kernel, cfg["name"]),
         },

@@ -57,7 +57,13 @@ constexpr int64_t kTcDirectTiles = 152 * 2;
 constexpr int kHiLoBelow = 512;
 constexpr float kHiLoScale = 1.25f;
 
-enum class Path { SplitBF16, SplitF32, TensorCore };
+// fp32 calls with at least this many columns (G x q_len) per (sequence, kv head)
+// take the 128-column tile kernel; its splits aim for about 8 waves of one CTA
+// per SM (its CTAs are long: 32-key blocks of 128 x D x 2 FFMA each).
+constexpr int kF32TileMinCols = 64;
+constexpr int64_t kF32TilePlanCtas = 152 * 8;
+
+enum class Path { SplitBF16, SplitF32, SplitF32Tile, TensorCore };
 
 struct Plan {
     Path path;
@@ -142,12 +148,22 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         return ATLAS_OK;
     }
     plan->path = L->kv_dtype == ATLAS_BF16 ? Path::SplitBF16 : Path::SplitF32;
-    const int cols = plan->path == Path::SplitBF16 ? split_bf16_cols_per_cta(G, L->q_len) : 8;
+    if (plan->path == Path::SplitF32 && (int64_t)G * L->q_len >= kF32TileMinCols)
+        plan->path = Path::SplitF32Tile;
+    const int cols = plan->path == Path::SplitBF16      ? split_bf16_cols_per_cta(G, L->q_len)
+                     : plan->path == Path::SplitF32Tile ? split_f32_tile_cols()
+                                                        : 8;
     plan->col_tiles = (G * L->q_len + cols - 1) / cols;
     if ((int64_t)Hkv * plan->col_tiles > 65535 || L->batch > 65535) return ATLAS_ERR_UNSUPPORTED;
 
     int64_t chunk = L->split_tokens;
-    if (chunk == 0) {
+    if (chunk == 0 && plan->path == Path::SplitF32Tile) {
+        const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
+        chunk = round_up((work_ctx * units + kF32TilePlanCtas - 1) / kF32TilePlanCtas,
+                         kSplitBlockTokens);
+        if (chunk < 512) chunk = 512;
+        if (chunk > 16384) chunk = 16384;
+    } else if (chunk == 0) {
         const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
         chunk = round_up((work_ctx * units + kPlanCtas - 1) / kPlanCtas, kSplitBlockTokens);
         // The f32 kernel has no pipeline to fill: small splits just add CTAs.
@@ -317,6 +333,8 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         if (st == ATLAS_OK) st = encode_pool_map(&tmV, v_pages, L->num_pages, Hkv, P, D);
         if (st != ATLAS_OK) return st;
         err = launch_split_bf16(sp, tmK, tmV, stream);
+    } else if (plan.path == Path::SplitF32Tile) {
+        err = launch_split_f32_tile(sp, stream);
     } else {
         err = launch_split_f32(sp, stream);
     }

@@ -105,6 +105,9 @@ int split_bf16_cols_per_cta(int G, int q_len);
 cudaError_t launch_split_bf16(const SplitParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               cudaStream_t stream);
 cudaError_t launch_split_f32(const SplitParams &p, cudaStream_t stream);
+// fp32 with many columns per (sequence, kv head): 128-column register-tiled FFMA.
+int split_f32_tile_cols();
+cudaError_t launch_split_f32_tile(const SplitParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 
 }  // namespace atlas
