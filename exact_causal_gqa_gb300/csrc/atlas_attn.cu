@@ -152,7 +152,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         plan->path = Path::SplitF32Tile;
     const int cols = plan->path == Path::SplitBF16      ? split_bf16_cols_per_cta(G, L->q_len)
                      : plan->path == Path::SplitF32Tile ? split_f32_tile_cols()
-                                                        : 8;
+                                                        : split_f32_cols_per_cta(G, L->q_len);
     plan->col_tiles = (G * L->q_len + cols - 1) / cols;
     if ((int64_t)Hkv * plan->col_tiles > 65535 || L->batch > 65535) return ATLAS_ERR_UNSUPPORTED;
 

@@ -104,6 +104,8 @@ int split_bf16_cols_per_cta(int G, int q_len);
 
 cudaError_t launch_split_bf16(const SplitParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               cudaStream_t stream);
+// fp32 with few columns: 4, 8 or 16 columns per CTA by G x q_len.
+int split_f32_cols_per_cta(int G, int q_len);
 cudaError_t launch_split_f32(const SplitParams &p, cudaStream_t stream);
 // fp32 with many columns per (sequence, kv head): 128-column register-tiled FFMA.
 int split_f32_tile_cols();

@@ -457,16 +457,35 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 }
 
 // ---------------------------------------------------------------- f32 path
-// Plain FFMA: each warp takes every 4th key of the split, lanes split the head
-// dimension, scores are warp all-reduces; up to 8 columns per CTA.
-template <int D>
-__global__ void __launch_bounds__(128)
+// Few columns per (sequence, kv head) in fp32 (decode, short suffixes).  Each of
+// the 8 warps streams its own 8-key K/V blocks (blocks w, w+8, ... of the split)
+// into a private double-buffered ring by cp.async and keeps its own online-softmax
+// state per column; the warps' states are combined at the end.  Scores: lane l
+// takes key l % 8 of the block and column group l / 8 (a quarter of the columns)
+// and forms whole D-long dot products from shared memory, so every score and
+// every exponential is computed once.  PV: lanes split the head dimension and read
+// P back from shared memory.  Keys past the split's end are zero-filled, never read.
+constexpr int kF32Keys = 8;
+
+template <int D, int NC>
+struct F32Layout {
+    static constexpr int W = 8;                           // warps per CTA
+    static constexpr int KS = D + 4;                      // padded row stride (floats)
+    static constexpr int kBuf = kF32Keys * KS;            // one K or V block
+    static constexpr int kWarp = 4 * kBuf + kF32Keys * NC;  // K[2], V[2], P[key][col]
+    static constexpr int kQ = NC * KS;
+    static constexpr int kBytes = (kQ + W * kWarp) * 4;
+    static_assert(2 * W * NC + W * NC * D <= W * kWarp, "combine scratch fits the rings");
+};
+
+template <int D, int NC>
+__global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, 1)
     split_f32_kernel(const SplitParams p) {
-    constexpr int NC = 8;
-    constexpr int W = 4;
-    constexpr int DPL = D / 32;
-    __shared__ float cm[W * NC], cl[W * NC];
-    __shared__ float cacc[W * NC * D];
+    using Lay = F32Layout<D, NC>;
+    constexpr int W = Lay::W, BK = kF32Keys, DPL = D / 32, NQ = NC / 4, DV4 = D / 4;
+    extern __shared__ __align__(16) float f32d_smem[];
+    float *sQ = f32d_smem;
+    float *sW = sQ + Lay::kQ;
 
     int L, kv_begin, kv_end, col0, ncols, qn;
     if (!split_prologue<NC>(p, blockIdx.y % p.col_tiles, L, kv_begin, kv_end, col0, ncols, qn))
@@ -476,75 +495,179 @@ __global__ void __launch_bounds__(128)
     const int hkv = blockIdx.y / p.col_tiles;
     const float *kp = static_cast<const float *>(p.k_pages);
     const float *vp = static_cast<const float *>(p.v_pages);
+    const int32_t *ptab = p.page_table + (int64_t)b * p.max_pages;
 
-    float qv[NC][DPL], accv[NC][DPL], m_run[NC], l_run[NC];
+    for (int idx = threadIdx.x; idx < NC * DV4; idx += W * 32) {
+        const int c = idx / DV4, d4 = idx % DV4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < ncols && (col0 + c) % p.q_len < qn)
+            v = reinterpret_cast<const float4 *>(static_cast<const float *>(p.q) +
+                                                 column_row(p, b, hkv, col0 + c) * D)[d4];
+        *reinterpret_cast<float4 *>(sQ + c * Lay::KS + 4 * d4) = v;
+    }
     int lim[NC], lo[NC];
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         const bool ok = c < ncols && (col0 + c) % p.q_len < qn;
-        const float *qrow = ok ? static_cast<const float *>(p.q) +
-                                     column_row(p, b, hkv, col0 + c) * D
-                               : nullptr;
-#pragma unroll
-        for (int j = 0; j < DPL; ++j) {
-            qv[c][j] = ok ? qrow[lane * DPL + j] : 0.f;
-            accv[c][j] = 0.f;
-        }
-        lim[c] = ok ? min(kv_end, column_visible(p, L, col0 + c)) : 0;
+        lim[c] = ok ? min(kv_end, column_visible(p, L, col0 + c)) : kv_begin;
         lo[c] = ok ? column_first(p, L, col0 + c) : 0;
-        m_run[c] = -INFINITY;
-        l_run[c] = 0.f;
     }
-    // Each warp takes 4 consecutive keys per step (its K/V rows are loaded
-    // together, so their memory latencies overlap) and every 4th such group.
-    constexpr int U = 4;
-    for (int t0 = kv_begin + warp * U; t0 < kv_end; t0 += W * U) {
-        float kr[U][DPL], vr[U][DPL];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int t = t0 + u;
-            if (t < kv_end) {
-                const int phys = p.page_table[(int64_t)b * p.max_pages + t / p.P];
-                const int64_t base =
-                    (((int64_t)phys * p.Hkv + hkv) * p.P + t % p.P) * D + lane * DPL;
-#pragma unroll
-                for (int j = 0; j < DPL; ++j) {
-                    kr[u][j] = kp[base + j];
-                    vr[u][j] = vp[base + j];
-                }
-            }
+    __syncthreads();
+
+    float *wK = sW + warp * Lay::kWarp;
+    float *wV = wK + 2 * Lay::kBuf;
+    float *wP = wK + 4 * Lay::kBuf;
+    auto load = [&](int kb, int buf) {
+        const uint32_t kd = smem_u32(wK + buf * Lay::kBuf), vd = smem_u32(wV + buf * Lay::kBuf);
+        for (int idx = lane; idx < BK * DV4; idx += 32) {
+            const int kr = idx / DV4, d4 = idx % DV4;
+            const int t = kb + kr;
+            const bool in = t < kv_end;
+            const int tt = in ? t : kv_begin;
+            const int64_t row = ((int64_t)ptab[tt / p.P] * p.Hkv + hkv) * p.P + tt % p.P;
+            const uint32_t off = (uint32_t)(kr * Lay::KS + 4 * d4) * 4u;
+            cp_async16(kd + off, kp + row * D + 4 * d4, in ? 16u : 0u);
+            cp_async16(vd + off, vp + row * D + 4 * d4, in ? 16u : 0u);
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int t = t0 + u;
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                if (t >= lim[c] || t < lo[c]) continue;  // warp-uniform (lim <= kv_end)
-                float dot = 0.f;
-#pragma unroll
-                for (int j = 0; j < DPL; ++j) dot = fmaf(qv[c][j], kr[u][j], dot);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                const float s2 = score_log2(p, dot);
-                const float m_new = fmaxf(m_run[c], s2);
-                const float corr = ex2(m_run[c] - m_new);
-                const float pw = ex2(s2 - m_new);
-                l_run[c] = l_run[c] * corr + pw;
-#pragma unroll
-                for (int j = 0; j < DPL; ++j) accv[c][j] = fmaf(pw, vr[u][j], accv[c][j] * corr);
-                m_run[c] = m_new;
-            }
-        }
-    }
+    };
+
+    float acc[NC][DPL], m_run[NC], l_part[NQ];
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        if (lane == 0) {
-            cm[warp * NC + c] = m_run[c];
-            cl[warp * NC + c] = l_run[c];
+        m_run[c] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[c][e] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) l_part[i] = 0.f;
+
+    const int nblk = (kv_end - kv_begin + BK - 1) / BK;
+    const int key = lane % BK, grp = lane / BK;
+    // limits of this lane's columns grp*NQ + i (selected with constant indices)
+    int limh[NQ], loh[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+        limh[i] = grp == 0 ? lim[i] : grp == 1 ? lim[NQ + i] : grp == 2 ? lim[2 * NQ + i]
+                                                                          : lim[3 * NQ + i];
+        loh[i] = grp == 0 ? lo[i] : grp == 1 ? lo[NQ + i] : grp == 2 ? lo[2 * NQ + i]
+                                                                     : lo[3 * NQ + i];
+    }
+    int j = warp;
+    if (j < nblk) load(kv_begin + j * BK, 0);
+    cp_async_commit();
+    for (int it = 0; j < nblk; ++it, j += W) {
+        const int kb = kv_begin + j * BK;
+        const int buf = it & 1;
+        if (j + W < nblk) load(kb + W * BK, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncwarp();
+        const float *cK = wK + buf * Lay::kBuf;
+        const float *cV = wV + buf * Lay::kBuf;
+
+        // scores of this lane's key for columns grp*NQ .. grp*NQ + NQ - 1
+        float s[NQ];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) s[i] = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < D; d += 4) {
+            const float4 k4 = *reinterpret_cast<const float4 *>(cK + key * Lay::KS + d);
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) {
+                const float4 q4 =
+                    *reinterpret_cast<const float4 *>(sQ + (grp * NQ + i) * Lay::KS + d);
+                s[i] = fmaf(q4.x, k4.x, s[i]);
+                s[i] = fmaf(q4.y, k4.y, s[i]);
+                s[i] = fmaf(q4.z, k4.z, s[i]);
+                s[i] = fmaf(q4.w, k4.w, s[i]);
+            }
+        }
+        const int t = kb + key;
+        float corr[NC];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            s[i] = (t < limh[i] && t >= loh[i]) ? score_log2(p, s[i]) : -INFINITY;
+            float mx = s[i];
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            // block maxima of columns g*NQ + i from the lanes of group g
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int cc = g * NQ + i;
+                const float m_new = fmaxf(m_run[cc], __shfl_sync(0xffffffffu, mx, g * BK));
+                const float mref = m_new == -INFINITY ? 0.f : m_new;
+                corr[cc] = ex2(m_run[cc] - mref);  // 0 while nothing was visible
+                m_run[cc] = m_new;
+            }
         }
 #pragma unroll
-        for (int j = 0; j < DPL; ++j) cacc[(warp * NC + c) * D + lane * DPL + j] = accv[c][j];
+        for (int i = 0; i < NQ; ++i) {
+            const float mr = grp == 0 ? m_run[i] : grp == 1 ? m_run[NQ + i]
+                             : grp == 2 ? m_run[2 * NQ + i] : m_run[3 * NQ + i];
+            const float cr = grp == 0 ? corr[i] : grp == 1 ? corr[NQ + i]
+                             : grp == 2 ? corr[2 * NQ + i] : corr[3 * NQ + i];
+            const float pv = ex2(s[i] - (mr == -INFINITY ? 0.f : mr));
+            l_part[i] = fmaf(l_part[i], cr, pv);
+            wP[key * NC + grp * NQ + i] = pv;
+        }
+        __syncwarp();
+        // O += P V, lanes over the head dimension
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[c][e] *= corr[c];
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            float pk[NC];
+#pragma unroll
+            for (int c4 = 0; c4 < NC; c4 += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(wP + kk * NC + c4);
+                pk[c4] = v.x;
+                pk[c4 + 1] = v.y;
+                pk[c4 + 2] = v.z;
+                pk[c4 + 3] = v.w;
+            }
+            float vv[DPL];
+            if (DPL == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(cV + kk * Lay::KS + lane * DPL);
+                vv[0] = v.x;
+                vv[1] = v.y;
+                vv[2 % DPL] = v.z;
+                vv[3 % DPL] = v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(cV + kk * Lay::KS + lane * DPL);
+                vv[0] = v.x;
+                vv[1] = v.y;
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[c][e] = fmaf(pk[c], vv[e], acc[c][e]);
+        }
+        __syncwarp();  // P and this buffer are rewritten by the next round
     }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+        l_part[i] += __shfl_xor_sync(0xffffffffu, l_part[i], 1);
+        l_part[i] += __shfl_xor_sync(0xffffffffu, l_part[i], 2);
+        l_part[i] += __shfl_xor_sync(0xffffffffu, l_part[i], 4);
+    }
+    __syncthreads();  // every warp is done with its ring: reuse it for the combine
+    float *cm = sW, *cl = sW + W * NC, *cacc = sW + 2 * W * NC;
+    if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) cm[warp * NC + c] = m_run[c];
+    }
+    if (key == 0) {
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) cl[warp * NC + grp * NQ + i] = l_part[i];
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) cacc[(warp * NC + c) * D + lane * DPL + e] = acc[c][e];
     __syncthreads();
     write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, false);
 }
@@ -803,11 +926,39 @@ cudaError_t launch_split_bf16(const SplitParams &p, const CUtensorMap &tmK, cons
                 : launch_bf16_instance<64, 1, 4>(p, tmK, tmV, stream);
 }
 
-cudaError_t launch_split_f32(const SplitParams &p, cudaStream_t stream) {
+template <int D, int NC>
+cudaError_t launch_f32_instance(const SplitParams &p, cudaStream_t stream) {
+    using Lay = F32Layout<D, NC>;
+    auto kern = split_f32_kernel<D, NC>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && !configured[dev]) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+        if (err != cudaSuccess) return err;
+        configured[dev] = 1;
+    }
     dim3 grid(p.n_chunks, p.Hkv * p.col_tiles, p.B);
-    if (p.D == 128) split_f32_kernel<128><<<grid, 128, 0, stream>>>(p);
-    else split_f32_kernel<64><<<grid, 128, 0, stream>>>(p);
+    kern<<<grid, Lay::W * 32, Lay::kBytes, stream>>>(p);
     return cudaGetLastError();
+}
+
+int split_f32_cols_per_cta(int G, int q_len) {
+    const int n = G * q_len;
+    return n <= 4 ? 4 : n <= 8 ? 8 : 16;
+}
+
+cudaError_t launch_split_f32(const SplitParams &p, cudaStream_t stream) {
+    const int nc = split_f32_cols_per_cta(p.G, p.q_len);
+    if (p.D == 128) {
+        return nc == 4   ? launch_f32_instance<128, 4>(p, stream)
+               : nc == 8 ? launch_f32_instance<128, 8>(p, stream)
+                         : launch_f32_instance<128, 16>(p, stream);
+    }
+    return nc == 4   ? launch_f32_instance<64, 4>(p, stream)
+           : nc == 8 ? launch_f32_instance<64, 8>(p, stream)
+                     : launch_f32_instance<64, 16>(p, stream);
 }
 
 template <int D>
