@@ -489,17 +489,28 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             // Outer loops stay rolled: a fully unrolled body overflows the
             // instruction cache shared with the producer and MMA warps.
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (all_visible) {
-#pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t sr[32];
-                    tmem_ld32(ts + cc * 32, sr);
-                    tmem_wait_ld();
+            auto max32 = [&](const uint32_t (&v)[32]) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2)
-                        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(sr[e]),
-                                                 __uint_as_float(sr[e + 1]));
-                }
+                for (int e = 0; e < 32; e += 2)
+                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[e]),
+                                             __uint_as_float(v[e + 1]));
+            };
+            if (all_visible) {
+                // Two 32-column buffers: the next quarter loads while this one is
+                // reduced (the waits name the loaded registers, so no use moves above).
+                uint32_t ma[32], mb[32];
+                tmem_ld32(ts, ma);
+                tmem_wait_ld32(ma);
+                tmem_ld32(ts + 32, mb);
+                max32(ma);
+                tmem_wait_ld32(mb);
+                tmem_ld32(ts + 64, ma);
+                max32(mb);
+                tmem_wait_ld32(ma);
+                tmem_ld32(ts + 96, mb);
+                max32(ma);
+                tmem_wait_ld32(mb);
+                max32(mb);
             } else {
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
