@@ -348,13 +348,15 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                         return false;
                     tc_fence_after();
                 }
-                const uint32_t kbase = sb + C::OFF_K + s * kTileBytes;
-                const uint32_t qbase = sb + C::OFF_Q + x * kTileBytes;
+                // Descriptors built once per operand base; the K slices step through
+                // the 14-bit address field (16-byte units), which no smem offset here
+                // can carry out of.
+                const uint64_t kd = sdesc_sw128(sb + C::OFF_K + s * kTileBytes, 16, 1024);
+                const uint64_t qd = sdesc_sw128(sb + C::OFF_Q + x * kTileBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-                    umma_bf16(tmem + C::s_col(x, j % SB), sdesc_sw128(qbase + off, 16, 1024),
-                              sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0);
+                    const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
+                    umma_bf16(tmem + C::s_col(x, j % SB), qd + off, kd + off, idS, kk > 0);
                 }
                 umma_commit(BAR(C::B_SFULL + x * SB + j % SB));
                 if (x == NT - 1) {
@@ -394,21 +396,21 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                         }
                     }
                     tc_fence_after();
-                    const uint32_t vbase = sb + C::OFF_V + s * kTileBytes;
+                    const uint64_t vd = sdesc_sw128(sb + C::OFF_V + s * kTileBytes, kSlab, 1024);
                     const uint32_t pcol = tmem + C::s_col(x, j % SB);
                     // keys 16kk .. 16kk+15 of P sit in columns (kk/4)*64 + (kk%4)*8 .. +8;
-                    // their remainders 32 columns further on.
+                    // their remainders 32 columns further on.  V slice kk starts 2048
+                    // bytes (128 descriptor units) after slice kk-1.
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         umma_bf16_tmem_a(tmem + C::o_col(x), pcol + (kk >> 2) * 64 + (kk & 3) * 8,
-                                         sdesc_sw128(vbase + kk * 2048, kSlab, 1024), idPV,
-                                         (j > 0 || kk > 0) ? 1u : 0u);
+                                         vd + kk * 128u, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                     if (hilo) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             umma_bf16_tmem_a(tmem + C::o_col(x),
                                              pcol + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
-                                             sdesc_sw128(vbase + kk * 2048, kSlab, 1024), idPV, 1u);
+                                             vd + kk * 128u, idPV, 1u);
                     }
                     umma_commit(BAR(C::B_PVDONE + x));
                     TRACE(1, 4 + 16 * x, j);
