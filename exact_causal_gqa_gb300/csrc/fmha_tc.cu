@@ -67,6 +67,13 @@ constexpr int kTileBytes = 128 * 128 * 2;  // a 128 x 128 bf16 tile (Q, K or V)
 constexpr int kSlab = 128 * 128;           // one 64-column slab of such a tile
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows 256x
+// A block takes P as bf16 hi + lo when, for some row of the tile, its largest weight
+// exceeds w = 1/20 of a lower bound of the row's total (sum so far + that weight).
+// Below it the single bf16 rounding of P stays well inside the 2e-3 bound (a CPU model
+// of the rounding: max error 9e-4 over rows whose largest final weight is <= 1/20, up
+// to 1.1e-2 above it, e.g. rows dominated by a few outlier keys).  The test runs in
+// the log domain against log2(w / (1 - w)) = log2(1/19).
+constexpr float kLog2HiLo = -4.2479275f;
 
 template <int NT>
 struct Cfg {
@@ -98,7 +105,10 @@ struct Cfg {
     static constexpr int kBars = B_FINAL + 1;
     static constexpr int OFF_TMEM = OFF_BAR + kBars * 8;
     static constexpr int OFF_FLAG = OFF_TMEM + 8;
-    static constexpr int kSmem = OFF_FLAG + 8 + 1024;  // + slack to align the base
+    // [NT][2] words of 4 bytes, one byte per warp of the tile: "this block needs P as
+    // hi + lo", double-buffered by block parity
+    static constexpr int OFF_VOTE = OFF_FLAG + 8;
+    static constexpr int kSmem = OFF_VOTE + NT * 8 + 1024;  // + slack to align the base
     static_assert(kSmem <= 232448, "shared memory budget");
     // TMEM columns: NT=2 -> [S0 | O0 | S1 | O1]; NT=1 -> [S(buf 0) | S(buf 1) | O]
     __device__ static constexpr uint32_t s_col(int x, int b) {
@@ -405,7 +415,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     for (int kk = 0; kk < 8; ++kk)
                         umma_bf16_tmem_a(tmem + C::o_col(x), pcol + (kk >> 2) * 64 + (kk & 3) * 8,
                                          vd + kk * 128u, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    if (hilo) {
+                    // The softmax's vote for this block (written before its P arrival),
+                    // read once the hi products are queued so its latency hides there.
+                    const bool split_blk =
+                        hilo || *reinterpret_cast<volatile uint32_t *>(
+                                    smem + C::OFF_VOTE + (x * 2 + (j & 1)) * 4) != 0u;
+                    if (split_blk) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             umma_bf16_tmem_a(tmem + C::o_col(x),
@@ -470,6 +485,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
         const uint32_t to = tl + C::o_col(x);
         float m_used = -INFINITY, l = 0.f;
+        float log2_l = -INFINITY;  // log2(l), refreshed at the end of each block
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
             const int bsel = j % SB;
@@ -537,12 +553,27 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const float mx = mraw == -INFINITY ? -INFINITY
                              : capped ? p.softcap_log2 * tanh_acc(mraw * p.softcap_inv)
                                       : mraw * p.scale_log2;
-            float corr = 1.f;
+            float corr = 1.f, log2_corr = 0.f;
             if (mx > m_used + kRescaleThreshold) {
-                corr = ex2(m_used - mx);  // 0 on the first visible block
+                log2_corr = m_used - mx;  // -inf on the first visible block
+                corr = ex2(log2_corr);    // 0 there
                 m_used = mx;
             }
             const float mref = m_used == -INFINITY ? 0.f : m_used;
+            // hi + lo P for this block?  Static per tile; else each warp decides for
+            // its 32 rows and leaves its vote for the MMA thread (read after this
+            // warp's P arrival), which multiplies the lo part when any warp of the
+            // tile asked for it.  A warp that did not ask writes zeros there.
+            bool split_blk = hilo;
+            if (!hilo) {
+                // largest weight maxp = 2^(mx - mref) against w (l corr + maxp), in the
+                // log domain (no exponential on this path): log2 maxp > log2(w / (1 - w))
+                // + log2 l + log2 corr.  l = 0 gives -inf on the right: always hi + lo.
+                const bool need = mx - mref > kLog2HiLo + log2_l + log2_corr;
+                split_blk = __any_sync(0xffffffffu, need);
+                if (lane == 0)
+                    smem[C::OFF_VOTE + (x * 2 + (j & 1)) * 4 + q4] = split_blk ? 1 : 0;
+            }
             if (r == 0) TRACE(2 + x, 3, j + 0 * (int)(mref != mref));
 
             // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs, written over columns
@@ -587,7 +618,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     }
                 }
             };
-            if (!hilo && all_visible && !capped) {
+            if (!split_blk && all_visible && !capped) {
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t sr[32], hw[16], lw[16];
@@ -603,17 +634,27 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     tmem_ld32(ts + h * 64, sr0);
                     tmem_ld32(ts + h * 64 + 32, sr1);
                     tmem_wait_ld();
-                    quarter(sr0, 2 * h, hw, lw, !all_visible, hilo, capped);
+                    quarter(sr0, 2 * h, hw, lw, !all_visible, split_blk, capped);
                     tmem_st16(ts + h * 64, hw);
-                    if (hilo) tmem_st16(ts + h * 64 + 32, lw);
-                    quarter(sr1, 2 * h + 1, hw, lw, !all_visible, hilo, capped);
+                    if (split_blk) tmem_st16(ts + h * 64 + 32, lw);
+                    quarter(sr1, 2 * h + 1, hw, lw, !all_visible, split_blk, capped);
                     tmem_st16(ts + h * 64 + 16, hw);
-                    if (hilo) tmem_st16(ts + h * 64 + 48, lw);
+                    if (split_blk) tmem_st16(ts + h * 64 + 48, lw);
                 }
+            }
+            if (!split_blk && !hilo) {
+                // lo columns (S of quarters 1 and 3, read by now) to zero, in case
+                // another warp of the tile asked for the lo product
+                uint32_t z[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) z[e] = 0u;
+                tmem_st32(ts + 32, z);
+                tmem_st32(ts + 96, z);
             }
             const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
             const float rs = (r01.x + r01.y) + (r23.x + r23.y);
             l = l * corr + rs;
+            log2_l = __log2f(l);  // for the next block's vote; -inf while l = 0
             if (r == 0) TRACE(2 + x, 6, j + 0 * (int)(l != l));
             // O must hold PV(j-1) before it is rescaled (and before PV(j) is issued,
             // which waits for this warpgroup's P).  Doing it after writing P keeps

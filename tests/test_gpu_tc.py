@@ -159,3 +159,13 @@ def test_tc_any_finite_scale(scale):
 def test_decode_any_finite_scale():
     prob = inputs.make("decode", 3, 16, 4, 128, 16, [5, 300, 2000], seed=9, scale=-0.2)
     check(prob)
+
+
+@pytest.mark.parametrize("kind,q_len,lens", [("prefill", 2048, [2048]), ("suffix", 64, [3000, 5000])])
+def test_late_score_jumps(kind, q_len, lens):
+    # K rows scaled x16 (about 0.2 % of keys) give later blocks scores far above the
+    # running max: the plain-path blocks after the first must rescale the P they
+    # already wrote with the old reference.
+    prob = inputs.make(kind, len(lens), 8, 2, 128, 64, lens, q_len=q_len, seed=21,
+                       k_outlier_prob=0.002, k_outlier_scale=16.0)
+    check(prob)
