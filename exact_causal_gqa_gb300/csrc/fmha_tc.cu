@@ -408,12 +408,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     tc_fence_after();
                     const uint64_t vd = sdesc_sw128(sb + C::OFF_V + s * kTileBytes, kSlab, 1024);
                     const uint32_t pcol = tmem + C::s_col(x, j % SB);
-                    // keys 16kk .. 16kk+15 of P sit in columns (kk/4)*64 + (kk%4)*8 .. +8;
-                    // their remainders 32 columns further on.  V slice kk starts 2048
+                    // keys 16kk .. 16kk+15 of P sit in columns 32*(kk/2) + 8*(kk%2) .. +8,
+                    // their remainders 16 columns further on.  V slice kk starts 2048
                     // bytes (128 descriptor units) after slice kk-1.
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16_tmem_a(tmem + C::o_col(x), pcol + (kk >> 2) * 64 + (kk & 3) * 8,
+                        umma_bf16_tmem_a(tmem + C::o_col(x), pcol + (kk >> 1) * 32 + (kk & 1) * 8,
                                          vd + kk * 128u, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                     // The softmax's vote for this block (written before its P arrival),
                     // read once the hi products are queued so its latency hides there.
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             umma_bf16_tmem_a(tmem + C::o_col(x),
-                                             pcol + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
+                                             pcol + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
                                              vd + kk * 128u, idPV, 1u);
                     }
                     umma_commit(BAR(C::B_PVDONE + x));
@@ -585,9 +585,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-mref, -mref);
             // Keys 2k, 2k+1 of quarter cc (columns 32cc..32cc+31 of S) -> P pair k,
-            // written to column 64*(cc/2) + 16*(cc%2) + k: always a column of S that
-            // has been read already.  The remainder goes 32 columns further on, so
-            // with the split the two quarters of a half are read before writing.
+            // written to column 32cc + k and its remainder (hi + lo blocks) to column
+            // 32cc + 16 + k: the quarter's own S columns, read just before.
             auto quarter = [&](const uint32_t (&sr)[32], int cc, uint32_t (&hw)[16],
                                uint32_t (&lw)[16], bool masked, bool split, bool cap) {
 #pragma unroll
@@ -618,6 +617,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     }
                 }
             };
+            // A warp that did not ask for hi + lo writes zeros over its lo columns, in
+            // case another warp of the tile did (then the MMA multiplies them).
+            uint32_t z16[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z16[e] = 0u;
             if (!split_blk && all_visible && !capped) {
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
@@ -625,31 +629,29 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     tmem_ld32(ts + cc * 32, sr);
                     tmem_wait_ld();
                     quarter(sr, cc, hw, lw, false, false, false);
-                    tmem_st16(ts + (cc >> 1) * 64 + (cc & 1) * 16, hw);
+                    tmem_st16(ts + cc * 32, hw);
+                    if (!hilo) tmem_st16(ts + cc * 32 + 16, z16);
+                }
+            } else if (all_visible && !capped) {
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32], hw[16], lw[16];
+                    tmem_ld32(ts + cc * 32, sr);
+                    tmem_wait_ld();
+                    quarter(sr, cc, hw, lw, false, true, false);
+                    tmem_st16(ts + cc * 32, hw);
+                    tmem_st16(ts + cc * 32 + 16, lw);
                 }
             } else {
 #pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t sr0[32], sr1[32], hw[16], lw[16];
-                    tmem_ld32(ts + h * 64, sr0);
-                    tmem_ld32(ts + h * 64 + 32, sr1);
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32], hw[16], lw[16];
+                    tmem_ld32(ts + cc * 32, sr);
                     tmem_wait_ld();
-                    quarter(sr0, 2 * h, hw, lw, !all_visible, split_blk, capped);
-                    tmem_st16(ts + h * 64, hw);
-                    if (split_blk) tmem_st16(ts + h * 64 + 32, lw);
-                    quarter(sr1, 2 * h + 1, hw, lw, !all_visible, split_blk, capped);
-                    tmem_st16(ts + h * 64 + 16, hw);
-                    if (split_blk) tmem_st16(ts + h * 64 + 48, lw);
+                    quarter(sr, cc, hw, lw, !all_visible, split_blk, capped);
+                    tmem_st16(ts + cc * 32, hw);
+                    tmem_st16(ts + cc * 32 + 16, split_blk ? lw : z16);
                 }
-            }
-            if (!split_blk && !hilo) {
-                // lo columns (S of quarters 1 and 3, read by now) to zero, in case
-                // another warp of the tile asked for the lo product
-                uint32_t z[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) z[e] = 0u;
-                tmem_st32(ts + 32, z);
-                tmem_st32(ts + 96, z);
             }
             const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
             const float rs = (r01.x + r01.y) + (r23.x + r23.y);
