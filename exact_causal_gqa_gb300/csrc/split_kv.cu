@@ -674,18 +674,21 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, 1)
 
 // ---------------------------------------------------------------- f32 tile path
 // Many query rows per (sequence, kv head) in fp32 (suffix, prefill): 128 columns
-// per CTA against 32-key blocks, both contractions as register-tiled FFMA.
+// per CTA against 64-key blocks, both contractions as register-tiled FFMA.
 // Warp w owns columns 16w .. 16w+15; lane (rg = lane / 8, kg = lane % 8) holds
-//   S for columns 16w + 4rg .. +3 and keys kg, kg+8, kg+16, kg+24 of the block,
+//   S for columns 16w + 4rg .. +3 and keys kg + 8c (c < 8) of the block,
 //   O for the same columns and dims 4kg + 32i .. +3 (i < D/32),
-// so a column's running max, sum and rescale stay within its 8 lanes.  K/V
-// blocks arrive by cp.async, double-buffered; keys past the split's end are
-// zero-filled (never read).  P goes through shared memory transposed
-// (P^T[key][column]) to the lanes that own the same columns' O.
-// Strides are padded by 4 floats so that the 16-byte reads of K, V and P^T
-// are free of bank conflicts; Q reads are quarter-warp broadcasts.
+// so a column's running max, sum and rescale stay within its 8 lanes.  K blocks
+// arrive by cp.async double-buffered; the single V buffer is refilled right after
+// the PV product and waited for just before the next one, so its load overlaps the
+// next scores.  Keys past the split's end are zero-filled (never read).  P goes
+// through shared memory transposed (P^T[key][column]) to the lanes that own the
+// same columns' O.  Strides are padded by 4 floats so that the 16-byte reads of K,
+// V and P^T are free of bank conflicts; Q reads are quarter-warp broadcasts.  The
+// kernel is bound by shared-memory wavefronts: the 4 x 8 S tile reads 12 of them
+// per 128 FMAs.
 constexpr int kF32TileCols = 128;
-constexpr int kF32TileKeys = 32;
+constexpr int kF32TileKeys = 64;
 constexpr int kF32TileThreads = 256;
 
 template <int D>
@@ -696,7 +699,8 @@ struct F32TileLayout {
     static constexpr int kQ = kF32TileCols * QS;
     static constexpr int kKV = kF32TileKeys * KS;     // one K or V block
     static constexpr int kP = kF32TileKeys * PS;
-    static constexpr int kBytes = (kQ + 4 * kKV + kP) * 4;
+    static constexpr int kBytes = (kQ + 3 * kKV + kP) * 4;  // Q, K[2], V, P^T
+    static_assert(kBytes <= 232448, "shared memory budget");
 };
 
 template <int D>
@@ -709,7 +713,7 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
     float *sQ = f32_smem;
     float *sK = sQ + Lay::kQ;
     float *sV = sK + 2 * Lay::kKV;
-    float *sP = sV + 2 * Lay::kKV;
+    float *sP = sV + Lay::kKV;
 
     // Prefill-shaped calls (q_len a multiple of the tile): late prompt rows, which
     // see the most keys, first.
@@ -749,19 +753,17 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
         lo[r] = valid[r] ? column_first(p, L, col0 + c) : 0;
     }
 
-    // One K/V block (keys kb .. kb+BK-1) into buffer `buf`.
-    auto load_block = [&](int kb, int buf) {
-        const uint32_t k_dst = smem_u32(sK + buf * Lay::kKV);
-        const uint32_t v_dst = smem_u32(sV + buf * Lay::kKV);
+    // Keys kb .. kb+BK-1 of K (into buffer buf) or V (the single V buffer).
+    auto load_rows = [&](const float *src, float *dst, int kb) {
+        const uint32_t d0 = smem_u32(dst);
         for (int idx = tid; idx < BK * DV4; idx += kF32TileThreads) {
             const int kr = idx / DV4, d4 = idx % DV4;
             const int t = kb + kr;
             const bool in = t < kv_end;
             const int tt = in ? t : kv_begin;
             const int64_t row = ((int64_t)ptab[tt / p.P] * p.Hkv + hkv) * p.P + tt % p.P;
-            const uint32_t off = (uint32_t)(kr * Lay::KS + 4 * d4) * 4u;
-            cp_async16(k_dst + off, kp + row * D + 4 * d4, in ? 16u : 0u);
-            cp_async16(v_dst + off, vp + row * D + 4 * d4, in ? 16u : 0u);
+            cp_async16(d0 + (uint32_t)(kr * Lay::KS + 4 * d4) * 4u, src + row * D + 4 * d4,
+                       in ? 16u : 0u);
         }
     };
 
@@ -776,36 +778,40 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
     }
 
     const int nb = (kv_end - kv_begin + BK - 1) / BK;
-    load_block(kv_begin, 0);
+    // cp.async groups, in commit order: K0, V0, then per block K(j+1) after the
+    // scores start and V(j+1) after the PV product; "all but the newest group
+    // complete" is then K(j) at the top of block j and V(j) before its PV product.
+    load_rows(kp, sK, kv_begin);
+    cp_async_commit();
+    load_rows(vp, sV, kv_begin);
     cp_async_commit();
     for (int j = 0; j < nb; ++j) {
         const int kb = kv_begin + j * BK;
-        if (j + 1 < nb) load_block(kb + BK, (j + 1) & 1);
-        cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
+        if (j + 1 < nb) load_rows(kp, sK + ((j + 1) & 1) * Lay::kKV, kb + BK);
+        cp_async_commit();
         const float *cK = sK + (j & 1) * Lay::kKV;
-        const float *cV = sV + (j & 1) * Lay::kKV;
 
-        // S = Q K^T for 4 columns x 4 keys
-        float s[4][4];
+        // S = Q K^T for 4 columns x 8 keys
+        float s[4][8];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) s[r][c] = 0.f;
-#pragma unroll 4
+            for (int c = 0; c < 8; ++c) s[r][c] = 0.f;
+#pragma unroll 2
         for (int d = 0; d < D; d += 4) {
-            float4 q4[4], k4[4];
+            float4 q4[4], k4[8];
 #pragma unroll
             for (int r = 0; r < 4; ++r)
                 q4[r] = *reinterpret_cast<const float4 *>(sQ + (r0 + r) * Lay::QS + d);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 8; ++c)
                 k4[c] = *reinterpret_cast<const float4 *>(cK + (kg + 8 * c) * Lay::KS + d);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     s[r][c] = fmaf(q4[r].x, k4[c].x, s[r][c]);
                     s[r][c] = fmaf(q4[r].y, k4[c].y, s[r][c]);
                     s[r][c] = fmaf(q4[r].z, k4[c].z, s[r][c]);
@@ -818,7 +824,7 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
         for (int r = 0; r < 4; ++r) {
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 const int t = kb + kg + 8 * c;
                 s[r][c] = (t < lim[r] && t >= lo[r]) ? score_log2(p, s[r][c]) : -INFINITY;
                 mx = fmaxf(mx, s[r][c]);
@@ -832,17 +838,16 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
             m_run[r] = m_new;
             float sum = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 s[r][c] = ex2(s[r][c] - mref);
                 sum += s[r][c];
             }
             l_part[r] = fmaf(l_part[r], corr[r], sum);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 8; ++c)
             *reinterpret_cast<float4 *>(sP + (kg + 8 * c) * Lay::PS + r0) =
                 make_float4(s[0][c], s[1][c], s[2][c], s[3][c]);
-        __syncwarp();
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -852,6 +857,8 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
                 o[r][i].z *= corr[r];
                 o[r][i].w *= corr[r];
             }
+        cp_async_wait<1>();  // V(j): every group but K(j+1)
+        __syncthreads();     // V(j) from every thread; P^T of this warp's columns
         // O += P V
 #pragma unroll 4
         for (int t = 0; t < BK; ++t) {
@@ -859,7 +866,8 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
             const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
             for (int i = 0; i < OD; ++i) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(cV + t * Lay::KS + 4 * kg + 32 * i);
+                const float4 v4 =
+                    *reinterpret_cast<const float4 *>(sV + t * Lay::KS + 4 * kg + 32 * i);
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     o[r][i].x = fmaf(pr[r], v4.x, o[r][i].x);
@@ -869,7 +877,9 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
                 }
             }
         }
-        __syncthreads();  // every warp is done with this buffer before it is refilled
+        __syncthreads();  // every warp is done with V (and this K buffer) before refills
+        if (j + 1 < nb) load_rows(vp, sV, kb + BK);
+        cp_async_commit();
     }
     cp_async_wait<0>();
 
