@@ -52,8 +52,9 @@ constexpr int64_t kTcPlanCtas = 152 * 3;
 constexpr int64_t kTcDirectTiles = 152 * 2;
 // Query tiles whose rows see fewer keys than this use a hi + lo split of P:
 // with few keys (or a peaked softmax) a single bf16 rounding of P moves the
-// output by up to 2^-9 |v|.  Scores sharper than unit-variance inputs at scale
-// 1/sqrt(D) (|scale| sqrt(D) above kHiLoScale) use the split on every tile.
+// output by up to 2^-8 |v| (bf16 keeps 8 significant bits).  Scores sharper than
+// unit-variance inputs at scale 1/sqrt(D) (|scale| sqrt(D) above kHiLoScale) use
+// the split on every tile.  Elsewhere the kernel decides per block (fmha_tc.cu).
 constexpr int kHiLoBelow = 512;
 constexpr float kHiLoScale = 1.25f;
 

@@ -115,3 +115,27 @@ def test_entry_points_check_arguments_before_any_launch(lib):
     args = [fake, fake, fake, fake, fake, 8, 2, 128, 16, ctypes.c_float(float("nan")),
             ctypes.byref(L)]
     assert lib.atlas_attn_decode(*args) == 1
+
+
+def split_tokens(lib, kind=0, Hq=8, Hkv=2, D=128, P=16, **kw):
+    L = launch(**kw)
+    return lib.atlas_attn_split_tokens(kind, Hq, Hkv, D, P, ctypes.byref(L))
+
+
+def test_split_tokens_and_phases(lib):
+    # the chunk size the pool's planner needs: the same as the plan's
+    assert split_tokens(lib, split_tokens=64) == 64
+    assert split_tokens(lib, split_tokens=64, phase=1) == 64
+    # invalid phase, invalid sizes
+    assert split_tokens(lib, phase=3) == -1
+    assert split_tokens(lib, Hq=7) == -1
+    assert lib.atlas_attn_workspace_size(0, 8, 2, 128, 16, ctypes.byref(launch(phase=7))) == SIZE_MAX
+    # a tensor-core call that would write its output directly has no chunks with
+    # phase ALL under the debug flag, and refuses the chunked phases then
+    tc = dict(q_len=64, batch=1, max_pages_per_seq=64, num_pages=64)
+    assert split_tokens(lib, kind=1, Hq=32, Hkv=4, debug_flags=atlas.DEBUG_TC_DIRECT, **tc) == 0
+    assert split_tokens(lib, kind=1, Hq=32, Hkv=4, debug_flags=atlas.DEBUG_TC_DIRECT, phase=1,
+                        **tc) == -1
+    # without the flag a chunked phase always gets chunks (multiples of 128 there)
+    n = split_tokens(lib, kind=1, Hq=32, Hkv=4, phase=1, **tc)
+    assert n > 0 and n % 128 == 0
