@@ -200,20 +200,35 @@ atlas_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, i
     return r == CUDA_SUCCESS ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 
-// 2-D view of a page pool: rows = num_pages*Hkv*P, D bf16 per row; boxes of
-// 64 elements x min(P, 64) rows with 128-byte swizzling.
+// View of a page pool (rows = num_pages*Hkv*P, D bf16 per row, 128-byte swizzle)
+// for the split kernel.  Pages of fewer than 64 tokens: a 3-D view [D/64 slabs]
+// [rows][64 elements] whose box is one page's P rows x all slabs, so one TMA load
+// brings a whole page (slab-major in shared memory: the 128-byte rows keep the
+// row & 7 swizzle).  This measured ~5 % faster than one box per slab at P = 16.
+// Larger pages: a 2-D view with boxes of 64 elements x 64 rows, one per slab.
 atlas_status encode_pool_map(CUtensorMap *map, const void *pool, int32_t num_pages, int32_t Hkv,
                              int32_t P, int32_t D) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return ATLAS_ERR_CUDA;
-    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_pages * Hkv * P};
-    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)(P < kSplitBlockTokens ? P : kSplitBlockTokens)};
-    const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t rows = (cuuint64_t)num_pages * Hkv * P;
+    CUresult r;
+    if (P < kSplitBlockTokens) {
+        const cuuint64_t dims[3] = {64u, rows, (cuuint64_t)D / 64};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128u};
+        const cuuint32_t box[3] = {64u, (cuuint32_t)P, (cuuint32_t)D / 64};
+        const cuuint32_t estr[3] = {1u, 1u, 1u};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+        const cuuint32_t box[2] = {64u, (cuuint32_t)kSplitBlockTokens};
+        const cuuint32_t estr[2] = {1u, 1u};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 

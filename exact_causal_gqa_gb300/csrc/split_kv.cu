@@ -9,8 +9,10 @@
 // with a structured merge).
 //
 // bf16 path, per CTA: one producer warp gathers the split's pages through the
-// page table with 2-D TMA loads (128-byte swizzle) into a STAGES-deep ring of
-// 64-key K/V blocks; four consumer warps each take 16 keys of every block and
+// page table with TMA loads (128-byte swizzle) into a STAGES-deep ring of
+// 64-key K/V blocks -- pages of fewer than 64 tokens come in one box per page
+// (a 3-D view [D/64 slabs][rows][64]), larger pages in one box per 64-column
+// slab; four consumer warps each take 16 keys of every block and
 // run both contractions on mma.sync tensor-core tiles with the keys on M:
 //   S^T[16 keys x 8 cols]  = K[16 x D] . Q^T[D x 8]      (ldmatrix from the ring)
 //   O^T[D x 8 cols]       += V^T[D x 16] . P^T[16 x 8]    (ldmatrix.trans; P^T via movmatrix)
@@ -159,6 +161,25 @@ __device__ void write_partials(const SplitParams &p, const float *cm, const floa
     }
 }
 
+// 3-D tiled TMA load into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map, int32_t x,
+                                                 int32_t y, int32_t z, uint32_t bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Byte offset of block row r (0..63) in the ring layout the producer writes:
+// rows come in boxes of 2^lg_br rows, each box holding all D/64 slabs of its rows.
+template <int D>
+__device__ __forceinline__ uint32_t box_row_offset(int r, int lg_br) {
+    const uint32_t box = (uint32_t)r >> lg_br, in_box = (uint32_t)r & ((1u << lg_br) - 1u);
+    return (((box << lg_br) * (D / 64)) + in_box) * 128u;
+}
+
 template <int D, int NT, int STAGES>
 struct SplitLayout {
     static constexpr int kTile = BT * D * 2;           // one 64-key K or V block, bf16
@@ -248,12 +269,19 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
                 __syncwarp((1u << nsub) - 1u);
                 const uint32_t kdst = sbase + s * Lay::kStage;
                 const uint32_t vdst = kdst + Lay::kTile;
+                if (BR < BT) {
+                    // One box per page: all D/64 slabs of its BR rows.
+                    const uint32_t off = (uint32_t)(lane * BR * (D / 64) * 128);
+                    tma_load_3d_hint(kdst + off, &tmK, 0, my_y, 0, full0 + 8 * s, policy);
+                    tma_load_3d_hint(vdst + off, &tmV, 0, my_y, 0, full0 + 8 * s, policy);
+                } else {
 #pragma unroll
-                for (int slab = 0; slab < D / 64; ++slab) {
-                    tma_load_2d_hint(kdst + slab * SLAB + lane * BR * 128, &tmK, slab * 64, my_y,
-                                     full0 + 8 * s, policy);
-                    tma_load_2d_hint(vdst + slab * SLAB + lane * BR * 128, &tmV, slab * 64, my_y,
-                                     full0 + 8 * s, policy);
+                    for (int slab = 0; slab < D / 64; ++slab) {
+                        tma_load_2d_hint(kdst + slab * SLAB, &tmK, slab * 64, my_y, full0 + 8 * s,
+                                         policy);
+                        tma_load_2d_hint(vdst + slab * SLAB, &tmV, slab * 64, my_y, full0 + 8 * s,
+                                         policy);
+                    }
                 }
             }
             __syncwarp();
@@ -308,6 +336,15 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[dt][nt][e] = 0.f;
 
+        // Ring layout of a block: box b (rows b*BR .. b*BR+BR-1) at b * BR * D/64 * 128
+        // bytes, slab-major inside (slab s at s * BR * 128), 128-byte rows swizzled by
+        // row & 7 (BR >= 8).  With BR = 64 this is the plain slab-major tile.
+        const int lg_br = 31 - __clz(p.P < BT ? p.P : BT);
+        const uint32_t slab_step = 128u << lg_br;
+        const int rk = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;  // K row of this lane
+        const int rv = 16 * warp + (lane & 7) + (lane >> 4) * 8;         // V row of this lane
+        const uint32_t row_k = box_row_offset<D>(rk, lg_br);
+        const uint32_t row_v = box_row_offset<D>(rv, lg_br);
         for (int j = 0; j < nblocks; ++j) {
             const int s = j % STAGES;
             // Warp-uniform decision: the mma.sync below needs every lane.
@@ -332,11 +369,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
                     for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
-                    const int r = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
                     const int d = kk * 16 + (lane >> 4) * 8;
                     uint32_t a[4];
-                    ldmatrix_x4(kt + (d / 64) * SLAB + sw128(r, (d % 64) / 8), a[0], a[1], a[2],
-                                a[3]);
+                    ldmatrix_x4(kt + row_k + (d / 64) * slab_step + ((((d % 64) / 8) ^ (rk & 7)) << 4),
+                                a[0], a[1], a[2], a[3]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, qf[kk][nt][0],
                                                                    qf[kk][nt][1]);
@@ -394,11 +430,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
                 }
 #pragma unroll
                 for (int dt = 0; dt < KSTEPS; ++dt) {
-                    const int key = 16 * warp + (lane & 7) + (lane >> 4) * 8;
                     const int d = dt * 16 + ((lane >> 3) & 1) * 8;
                     uint32_t a[4];
-                    ldmatrix_x4_trans(vt + (d / 64) * SLAB + sw128(key, (d % 64) / 8), a[0], a[1],
-                                      a[2], a[3]);
+                    ldmatrix_x4_trans(vt + row_v + (d / 64) * slab_step +
+                                          ((((d % 64) / 8) ^ (rv & 7)) << 4),
+                                      a[0], a[1], a[2], a[3]);
                     // Keys past the split end may hold stale or NaN rows: zero them.
                     a[0] &= keep01;
                     a[1] &= keep01;
