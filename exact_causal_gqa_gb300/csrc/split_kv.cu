@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 
 // ---------------------------------------------------------------- f32 path
 // Few columns per (sequence, kv head) in fp32 (decode, short suffixes).  Each of
-// the 8 warps streams its own 8-key K/V blocks (blocks w, w+8, ... of the split)
+// the W warps streams its own 8-key K/V blocks (blocks w, w+W, ... of the split)
 // into a private double-buffered ring by cp.async and keeps its own online-softmax
 // state per column; the warps' states are combined at the end.  Scores: lane l
 // takes key l % 8 of the block and column group l / 8 (a quarter of the columns)
@@ -505,7 +505,13 @@ constexpr int kF32Keys = 8;
 
 template <int D, int NC>
 struct F32Layout {
-    static constexpr int W = 8;                           // warps per CTA
+    // Warps per CTA and CTAs per SM: each warp holds ~17 KB of rings (D = 128), so
+    // 4-warp CTAs three to an SM keep 12 warps resident where 8-warp CTAs fit one;
+    // the kernel is latency-bound (dependent shuffles, exponentials and shared-memory
+    // round trips per 8-key block), and 12 warps measured 25-31 % faster than 8.
+    // 16 columns need ~205 registers a thread, more than three CTAs allow.
+    static constexpr int W = NC == 16 ? 8 : 4;
+    static constexpr int kMinCtas = NC == 16 ? 1 : 3;
     static constexpr int KS = D + 4;                      // padded row stride (floats)
     static constexpr int kBuf = kF32Keys * KS;            // one K or V block
     static constexpr int kWarp = 4 * kBuf + kF32Keys * NC;  // K[2], V[2], P[key][col]
@@ -515,7 +521,7 @@ struct F32Layout {
 };
 
 template <int D, int NC>
-__global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, 1)
+__global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kMinCtas)
     split_f32_kernel(const SplitParams p) {
     using Lay = F32Layout<D, NC>;
     constexpr int W = Lay::W, BK = kF32Keys, DPL = D / 32, NQ = NC / 4, DV4 = D / 4;
@@ -601,10 +607,13 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, 1)
         const float *cK = wK + buf * Lay::kBuf;
         const float *cV = wV + buf * Lay::kBuf;
 
-        // scores of this lane's key for columns grp*NQ .. grp*NQ + NQ - 1
-        float s[NQ];
+        // scores of this lane's key for columns grp*NQ .. grp*NQ + NQ - 1, each as four
+        // partial sums (d mod 4) so that the FMAs form 4*NQ independent chains
+        float s4[NQ][4];
 #pragma unroll
-        for (int i = 0; i < NQ; ++i) s[i] = 0.f;
+        for (int i = 0; i < NQ; ++i)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s4[i][u] = 0.f;
 #pragma unroll 8
         for (int d = 0; d < D; d += 4) {
             const float4 k4 = *reinterpret_cast<const float4 *>(cK + key * Lay::KS + d);
@@ -612,12 +621,15 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, 1)
             for (int i = 0; i < NQ; ++i) {
                 const float4 q4 =
                     *reinterpret_cast<const float4 *>(sQ + (grp * NQ + i) * Lay::KS + d);
-                s[i] = fmaf(q4.x, k4.x, s[i]);
-                s[i] = fmaf(q4.y, k4.y, s[i]);
-                s[i] = fmaf(q4.z, k4.z, s[i]);
-                s[i] = fmaf(q4.w, k4.w, s[i]);
+                s4[i][0] = fmaf(q4.x, k4.x, s4[i][0]);
+                s4[i][1] = fmaf(q4.y, k4.y, s4[i][1]);
+                s4[i][2] = fmaf(q4.z, k4.z, s4[i][2]);
+                s4[i][3] = fmaf(q4.w, k4.w, s4[i][3]);
             }
         }
+        float s[NQ];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) s[i] = (s4[i][0] + s4[i][1]) + (s4[i][2] + s4[i][3]);
         const int t = kb + key;
         float corr[NC];
 #pragma unroll
