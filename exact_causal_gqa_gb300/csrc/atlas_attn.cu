@@ -43,6 +43,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // always gets the same split (and the same bits).
 constexpr int64_t kPlanCtas = 152 * 2 * 2;
 constexpr int64_t kMaxSplit = 2560;
+// The fp32 ring kernel with 4 or 8 columns runs 4-warp CTAs three to an SM: its
+// splits aim for 152 x 3 x 4 CTAs, so that a small batch still fills every slot
+// (a lone 4-warp CTA on an SM runs at about half the rate of 12 warps).
+constexpr int64_t kF32RingPlanCtas = 152 * 3 * 4;
 
 // The tensor-core path's split plan aims for 152 SMs x 1 CTA x 3 waves at the
 // largest context (splits of 1K-8K keys; 8K measured best for the suffix
@@ -166,7 +170,9 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         if (chunk > 16384) chunk = 16384;
     } else if (chunk == 0) {
         const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
-        chunk = round_up((work_ctx * units + kPlanCtas - 1) / kPlanCtas, kSplitBlockTokens);
+        const int64_t target =
+            plan->path == Path::SplitF32 && cols <= 8 ? kF32RingPlanCtas : kPlanCtas;
+        chunk = round_up((work_ctx * units + target - 1) / target, kSplitBlockTokens);
         // The f32 kernel has no pipeline to fill: small splits just add CTAs.
         const int64_t min_chunk = plan->path == Path::SplitF32 ? kSplitBlockTokens : 512;
         if (chunk > kMaxSplit) chunk = kMaxSplit;
