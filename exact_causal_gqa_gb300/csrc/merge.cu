@@ -15,6 +15,7 @@ namespace atlas {
 namespace {
 
 constexpr int kRowsPerCta = 4;
+constexpr int kGroup = 8;  // splits whose loads are in flight together
 
 template <int D>
 __global__ void __launch_bounds__(kRowsPerCta * 32) merge_kernel(const MergeParams p) {
@@ -60,20 +61,40 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) merge_kernel(const MergePara
             for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
             float lsum = p.sinks ? ex2(sink2 - M) : 0.f;
             const float *wa = p.ws_acc + row * p.n_chunks * D + lane * DPL;
-            for (int s = first; s < nsplit; ++s) {
-                const float m = ml[2 * s], l = ml[2 * s + 1];
-                const float w = l > 0.f ? ex2(m - M) : 0.f;
-                lsum = fmaf(w, l, lsum);
-                if (DPL == 4) {
-                    const float4 a = *reinterpret_cast<const float4 *>(wa + (int64_t)s * D);
-                    acc[0] = fmaf(w, a.x, acc[0]);
-                    acc[1] = fmaf(w, a.y, acc[1]);
-                    acc[2] = fmaf(w, a.z, acc[2]);
-                    acc[3] = fmaf(w, a.w, acc[3]);
-                } else {
-                    const float2 a = *reinterpret_cast<const float2 *>(wa + (int64_t)s * D);
-                    acc[0] = fmaf(w, a.x, acc[0]);
-                    acc[1] = fmaf(w, a.y, acc[1]);
+            // Splits in groups of kGroup: every load of a group is issued before its
+            // first use, so a row costs one round trip to L2 per group, not per split.
+            // The sums run in split order as before.
+            for (int s0 = first; s0 < nsplit; s0 += kGroup) {
+                float m[kGroup], l[kGroup], a[kGroup][DPL];
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    const int s = s0 + u;
+                    m[u] = l[u] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < DPL; ++j) a[u][j] = 0.f;
+                    if (s < nsplit) {
+                        m[u] = ml[2 * s];
+                        l[u] = ml[2 * s + 1];
+                        if (DPL == 4) {
+                            const float4 v = *reinterpret_cast<const float4 *>(wa + (int64_t)s * D);
+                            a[u][0] = v.x;
+                            a[u][1] = v.y;
+                            a[u][2 % DPL] = v.z;
+                            a[u][3 % DPL] = v.w;
+                        } else {
+                            const float2 v = *reinterpret_cast<const float2 *>(wa + (int64_t)s * D);
+                            a[u][0] = v.x;
+                            a[u][1] = v.y;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    if (s0 + u >= nsplit) break;
+                    const float w = l[u] > 0.f ? ex2(m[u] - M) : 0.f;
+                    lsum = fmaf(w, l[u], lsum);
+#pragma unroll
+                    for (int j = 0; j < DPL; ++j) acc[j] = fmaf(w, a[u][j], acc[j]);
                 }
             }
 #pragma unroll
