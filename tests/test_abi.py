@@ -139,3 +139,31 @@ def test_split_tokens_and_phases(lib):
     # without the flag a chunked phase always gets chunks (multiples of 128 there)
     n = split_tokens(lib, kind=1, Hq=32, Hkv=4, phase=1, **tc)
     assert n > 0 and n % 128 == 0
+
+
+def test_split_plan_sizes(lib):
+    """The automatic split sizes are a pure function of the call's sizes: bf16 decode
+    aims for 152 x 2 x 2 CTAs, the fp32 ring kernel with 4 or 8 columns (4-warp CTAs,
+    three per SM) for 152 x 3 x 4, both capped at 2560 keys and rounded to 64."""
+    f32 = dict(q_dtype=0, kv_dtype=0, out_dtype=0)
+
+    def plan(batch, Hq, Hkv, ctx, P=16, **kw):
+        pages = ctx // P
+        return split_tokens(lib, Hq=Hq, Hkv=Hkv, P=P, batch=batch, max_pages_per_seq=pages,
+                            num_pages=batch * pages, **kw)
+
+    def expect(units, ctx, target):
+        chunk = -(-(-(-ctx * units // target)) // 64) * 64
+        return min(max(chunk, 64), 2560)
+
+    # bf16 GQA decode, 32 x 8 (sequence, kv head) units at 32K keys: the cap
+    assert plan(32, 32, 8, 32768) == 2560
+    assert plan(4, 32, 8, 32768) == max(512, expect(32, 32768, 608))
+    # fp32, 4 columns (G = 4): 1824-CTA target
+    assert plan(4, 32, 8, 32768, **f32) == expect(32, 32768, 1824) == 576
+    assert plan(1, 32, 8, 32768, **f32) == expect(8, 32768, 1824) == 192
+    assert plan(32, 32, 8, 32768, **f32) == 2560
+    # fp32, 8 columns (G = 8), long context
+    assert plan(4, 64, 8, 131072, P=64, **f32) == expect(32, 131072, 1824) == 2304
+    # fp32, 16 columns (G = 16): 8-warp CTAs, the 608-CTA target
+    assert plan(2, 32, 2, 16384, **f32) == expect(4, 16384, 608) == 128
