@@ -78,6 +78,8 @@ def test_workspace_size_matches_the_split_layout(lib):
     rows, splits, D = 2 * 8, 2, 128
     acc = rows * splits * D * 4
     assert n == (acc + 255) // 256 * 256 + rows * splits * 2 * 4
+    # fp32 K/V: the same layout
+    assert ws(lib, split_tokens=64, q_dtype=0, kv_dtype=0, out_dtype=0) == n
 
 
 @pytest.mark.parametrize("kw,expect", [
