@@ -169,3 +169,22 @@ def test_split_plan_sizes(lib):
     assert plan(4, 64, 8, 131072, P=64, **f32) == expect(32, 131072, 1824) == 2304
     # fp32, 16 columns (G = 16): 8-warp CTAs, the 608-CTA target
     assert plan(2, 32, 2, 16384, **f32) == expect(4, 16384, 608) == 128
+
+
+def test_tensor_core_plan_sizes(lib):
+    """Tensor-core calls (bf16, G * q_len > 16): splits of 1024-8192 keys in multiples of
+    128, aiming for 152 x 3 CTAs; prefill with at least 304 query tiles writes the output
+    directly (no chunks)."""
+    def plan(kind, batch, Hq, Hkv, q_len, ctx, P):
+        pages = ctx // P
+        return split_tokens(lib, kind=kind, Hq=Hq, Hkv=Hkv, P=P, batch=batch, q_len=q_len,
+                            max_pages_per_seq=pages, num_pages=batch * pages)
+
+    # suffix of 16 rows, G = 8, contexts up to 64K keys: 64 tiles -> the 8192-key cap
+    assert plan(1, 16, 32, 4, 16, 65536, 32) == 8192
+    # one short suffix: the 1024-key floor
+    assert plan(1, 1, 32, 4, 16, 4096, 32) == 1024
+    # causal prefill of 2 x 8192 rows, 32 / 8 heads: 4096 tiles, direct
+    assert plan(2, 2, 32, 8, 8192, 8192, 64) == 0
+    # a small prefill (64 tiles) is split, capped at its own length
+    assert plan(2, 1, 8, 2, 1024, 1024, 64) == 1024
