@@ -147,6 +147,16 @@ def kernel_source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def workload_traffic(args, kernel: str, workload: str):
+    """traffic_record for the named workload as the committed capture measured it; None
+    when this run changes the workload (batch, window, softcap, sinks, ragged rows or a
+    fixed split size), whose per-launch DRAM bytes that record does not describe."""
+    if args.batch or args.window or args.softcap or args.sinks or args.ragged or \
+            args.split_tokens:
+        return None
+    return traffic_record(kernel, workload)
+
+
 def traffic_record(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
     kernel source is unchanged since it was captured; else None."""
@@ -416,7 +426,7 @@ def run_atlas(args, world, rank, local):
             "peak_source": pk_kind,
             "unit": "TFLOP/s" if f32_tile else unit,
             "frac": round(achieved / peak, 4),
-            "traffic": traffic_record(kernel, cfg["name"]),
+            "traffic": workload_traffic(args, kernel, cfg["name"]),
         },
         "gpu_launches": launches_per_step * args.steps,
         "device_status": status_val,

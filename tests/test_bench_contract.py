@@ -47,3 +47,20 @@ def test_reference_arm_other_ranks_print_nothing():
     lines = run_bench("--impl", "reference", "--config", "1", "--steps", "1", "--warmup", "1",
                       env={"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"})
     assert lines == []
+
+
+def test_traffic_is_reported_only_for_the_captured_workload():
+    """The committed DRAM-traffic records describe the unmodified workloads; a run that
+    changes the workload reports traffic null rather than another workload's bytes."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    name = "gqa_decode_bf16_b32_h32x8_d128_ctx1k-32k_p16"
+    base = dict(batch=0, window=0, softcap=0.0, sinks=False, ragged=False, split_tokens=0)
+    plain = argparse.Namespace(**base)
+    assert bench.workload_traffic(plain, "split_bf16_kernel", name) == \
+        bench.traffic_record("split_bf16_kernel", name)
+    for change in (dict(batch=8), dict(window=4096), dict(softcap=30.0), dict(sinks=True),
+                   dict(ragged=True), dict(split_tokens=2048)):
+        args = argparse.Namespace(**{**base, **change})
+        assert bench.workload_traffic(args, "split_bf16_kernel", name) is None, change
