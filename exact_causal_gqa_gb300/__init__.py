@@ -59,7 +59,8 @@ class _Launch(ctypes.Structure):
                 ("debug_flags", ctypes.c_uint32), ("events", ctypes.c_void_p),
                 ("window", ctypes.c_int32), ("softcap", ctypes.c_float),
                 ("sinks", ctypes.c_void_p), ("q_lens", ctypes.c_void_p),
-                ("chunk_range", ctypes.c_void_p), ("phase", ctypes.c_int32)]
+                ("chunk_range", ctypes.c_void_p), ("phase", ctypes.c_int32),
+                ("sm_count", ctypes.c_int32)]
 
 PHASE_ALL, PHASE_CHUNKS, PHASE_MERGE = 0, 1, 2
 

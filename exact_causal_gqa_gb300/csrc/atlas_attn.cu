@@ -9,6 +9,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 namespace atlas {
@@ -37,23 +38,22 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // CTAs the automatic split plan aims for at the largest context the page table
-// allows: 152 SMs x 2 resident CTAs x 2 waves, with splits of at most
-// kMaxSplit keys (measured best at 2.5K-4K keys, ~1.3-2 MB of K/V per CTA, on the
-// decode workloads).  A pure function of the call's sizes, so a given problem
-// always gets the same split (and the same bits).
-constexpr int64_t kPlanCtas = 152 * 2 * 2;
+// allows: SMs x 2 resident CTAs x 2 waves, with splits of at most kMaxSplit keys
+// (measured best at 2.5K-4K keys, ~1.3-2 MB of K/V per CTA, on the decode
+// workloads).  A pure function of the call's sizes and the SM count, so a given
+// problem on a given part always gets the same split (and the same bits).
+int64_t plan_ctas(int sms) { return (int64_t)sms * 2 * 2; }
 constexpr int64_t kMaxSplit = 2560;
 // The fp32 ring kernel with 4 or 8 columns runs 4-warp CTAs three to an SM: its
-// splits aim for 152 x 3 x 4 CTAs, so that a small batch still fills every slot
+// splits aim for SMs x 3 x 4 CTAs, so that a small batch still fills every slot
 // (a lone 4-warp CTA on an SM runs at about half the rate of 12 warps).
-constexpr int64_t kF32RingPlanCtas = 152 * 3 * 4;
+int64_t f32_ring_plan_ctas(int sms) { return (int64_t)sms * 3 * 4; }
 
-// The tensor-core path's split plan aims for 152 SMs x 1 CTA x 3 waves at the
-// largest context (splits of 1K-8K keys; 8K measured best for the suffix
-// workload); it writes the output directly once a call has at least
-// kTcDirectTiles query tiles.
-constexpr int64_t kTcPlanCtas = 152 * 3;
-constexpr int64_t kTcDirectTiles = 152 * 2;
+// The tensor-core path's split plan aims for SMs x 1 CTA x 3 waves at the largest
+// context (splits of 1K-8K keys; 8K measured best for the suffix workload); it
+// writes the output directly once a call has at least SMs x 2 query tiles.
+int64_t tc_plan_ctas(int sms) { return (int64_t)sms * 3; }
+int64_t tc_direct_tiles(int sms) { return (int64_t)sms * 2; }
 // Query tiles whose rows see fewer keys than this use a hi + lo split of P:
 // with few keys (or a peaked softmax) a single bf16 rounding of P moves the
 // output by up to 2^-8 |v| (bf16 keeps 8 significant bits).  Scores sharper than
@@ -66,22 +66,39 @@ constexpr float kHiLoScale = 1.25f;
 // take the 128-column tile kernel; its splits aim for about 8 waves of one CTA
 // per SM (its CTAs are long: 32-key blocks of 128 x D x 2 FFMA each).
 constexpr int kF32TileMinCols = 64;
-constexpr int64_t kF32TilePlanCtas = 152 * 8;
+int64_t f32_tile_plan_ctas(int sms) { return (int64_t)sms * 8; }
 
-enum class Path { SplitBF16, SplitF32, SplitF32Tile, TensorCore };
-
-struct Plan {
-    Path path;
-    int chunk, n_chunks, col_tiles, G;
-    int tc_split, tiles_per_unit, tiles_per_head;
-    size_t acc_bytes, ml_offset, ws_bytes;
-};
+// One GB300: the count the plan assumes when no device is visible.
+constexpr int kDefaultSms = 152;
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+std::atomic<int> g_sm_count[64];
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return kDefaultSms;
+    }
+    const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return kDefaultSms;
+    }
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int32_t P,
                        const atlas_launch *L, Plan *plan) {
     if (!L) return ATLAS_ERR_INVALID_ARG;
+    if (L->sm_count < 0) return ATLAS_ERR_INVALID_ARG;
+    const int sms = L->sm_count > 0 ? L->sm_count : device_sm_count();
     if (kind != ATLAS_KIND_DECODE && kind != ATLAS_KIND_SUFFIX && kind != ATLAS_KIND_PREFILL)
         return ATLAS_ERR_INVALID_ARG;
     if (L->batch < 1 || L->max_pages_per_seq < 1 || L->num_pages < 1 || L->q_len < 1 || Hq < 1 ||
@@ -128,9 +145,10 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         int64_t chunk = 0;
         if (L->split_tokens > 0) {
             chunk = round_up(L->split_tokens, 128);
-        } else if ((tiles < kTcDirectTiles || L->phase != ATLAS_PHASE_ALL) &&
+        } else if ((tiles < tc_direct_tiles(sms) || L->phase != ATLAS_PHASE_ALL) &&
                    !(L->debug_flags & ATLAS_DEBUG_TC_DIRECT)) {
-            chunk = round_up((work_ctx * tiles + kTcPlanCtas - 1) / kTcPlanCtas, 128);
+            const int64_t target = tc_plan_ctas(sms);
+            chunk = round_up((work_ctx * tiles + target - 1) / target, 128);
             if (chunk < 1024) chunk = 1024;
             if (chunk > 8192) chunk = 8192;
         }
@@ -164,14 +182,14 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     int64_t chunk = L->split_tokens;
     if (chunk == 0 && plan->path == Path::SplitF32Tile) {
         const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
-        chunk = round_up((work_ctx * units + kF32TilePlanCtas - 1) / kF32TilePlanCtas,
-                         kSplitBlockTokens);
+        const int64_t target = f32_tile_plan_ctas(sms);
+        chunk = round_up((work_ctx * units + target - 1) / target, kSplitBlockTokens);
         if (chunk < 512) chunk = 512;
         if (chunk > 16384) chunk = 16384;
     } else if (chunk == 0) {
         const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
         const int64_t target =
-            plan->path == Path::SplitF32 && cols <= 8 ? kF32RingPlanCtas : kPlanCtas;
+            plan->path == Path::SplitF32 && cols <= 8 ? f32_ring_plan_ctas(sms) : plan_ctas(sms);
         chunk = round_up((work_ctx * units + target - 1) / target, kSplitBlockTokens);
         // The f32 kernel has no pipeline to fill: small splits just add CTAs.
         const int64_t min_chunk = plan->path == Path::SplitF32 ? kSplitBlockTokens : 512;
@@ -188,6 +206,8 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     plan->ws_bytes = plan->ml_offset + (size_t)rows * plan->n_chunks * 2 * sizeof(float);
     return ATLAS_OK;
 }
+
+namespace {
 
 // 2-D view of a bf16 tensor with D elements per row: `rows` rows; boxes of 64
 // elements x box_rows rows with 128-byte swizzling.

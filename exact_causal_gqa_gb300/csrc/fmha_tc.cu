@@ -34,30 +34,6 @@
 
 #include <math.h>
 
-// Compile-time timeline hooks for profiling builds (-DATLAS_TRACE): one CTA
-// records (clock64, role, event, block) tuples into a device array that the
-// profiling build reads back.  Compiled out of the library.
-#ifdef ATLAS_TRACE
-__device__ unsigned long long g_atlas_trace[8 * 16 * 512];  // [role][event][block]
-__device__ int g_atlas_trace_cta;
-#define TRACE(role, ev, j)                                                             \
-    do {                                                                               \
-        if ((int)(blockIdx.x + blockIdx.y * gridDim.x) == g_atlas_trace_cta && (j) < 512) \
-            g_atlas_trace[((role) * 16 + (ev)) * 512 + (j)] = clock64();               \
-    } while (0)
-extern "C" int atlas_trace_read(unsigned long long *host, int cta) {
-    if (host) cudaMemcpyFromSymbol(host, g_atlas_trace, sizeof(g_atlas_trace));
-    static unsigned long long zeros[8 * 16 * 512];
-    cudaMemcpyToSymbol(g_atlas_trace, zeros, sizeof(zeros));
-    cudaMemcpyToSymbol(g_atlas_trace_cta, &cta, sizeof(cta));
-    return 0;
-}
-#else
-#define TRACE(role, ev, j) \
-    do {                   \
-    } while (0)
-#endif
-
 namespace atlas {
 namespace {
 
@@ -328,7 +304,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 __syncwarp();
                 if (kv == 0) issued_k = j + 1;
                 else issued_v = j + 1;
-                TRACE(0, kv, j);
             }
         }
         if (failed && lane == 0) {
@@ -371,7 +346,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 umma_commit(BAR(C::B_SFULL + x * SB + j % SB));
                 if (x == NT - 1) {
                     umma_commit(BAR(C::B_KEMPTY + s));
-                    TRACE(1, 1, j);
                 }
                 return true;
             };
@@ -383,12 +357,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 const int s = j % S;
 #pragma unroll
                 for (int x = 0; x < NT; ++x) {
-                    TRACE(1, 2 + 16 * x, j);
                     if (!mbar_wait_bounded(BAR(C::B_PFULL + x), j & 1, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                    TRACE(1, 3 + 16 * x, j);
                     if (x == 0) {
                         if (!mbar_wait_bounded(BAR(C::B_VFULL + s), (j / S) & 1, abort_flag,
                                                kWaitLimitNs)) {
@@ -428,7 +400,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                                              vd + kk * 128u, idPV, 1u);
                     }
                     umma_commit(BAR(C::B_PVDONE + x));
-                    TRACE(1, 4 + 16 * x, j);
                     // Ping-pong: S_x(j + SB) follows PV_x(j) at once, so tile x starts
                     // its next softmax while the other tile's P is still being made.
                     // It writes the S buffer that PV_x(j) reads P_x(j) from; the
@@ -489,12 +460,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
             const int bsel = j % SB;
-            if (r == 0) TRACE(2 + x, 1, j);
             if (!wait_warp(BAR(C::B_SFULL + x * SB + bsel), (j / SB) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
-            if (r == 0) TRACE(2 + x, 2, j);
             tc_fence_after();
             const uint32_t ts = tl + C::s_col(x, bsel);
             const int nvis = lim_row - (kv_begin + j * BN);  // visible columns: [nlo, nvis)
@@ -574,11 +543,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 if (lane == 0)
                     smem[C::OFF_VOTE + (x * 2 + (j & 1)) * 4 + q4] = split_blk ? 1 : 0;
             }
-            if (r == 0) TRACE(2 + x, 3, j + 0 * (int)(mref != mref));
 
             // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs, written over columns
             // of S already read (see quarter() below), and the row sum.
-            if (r == 0) TRACE(2 + x, 5, j);
             float2 rs2[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) rs2[k] = make_float2(0.f, 0.f);
@@ -657,7 +624,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const float rs = (r01.x + r01.y) + (r23.x + r23.y);
             l = l * corr + rs;
             log2_l = __log2f(l);  // for the next block's vote; -inf while l = 0
-            if (r == 0) TRACE(2 + x, 6, j + 0 * (int)(l != l));
             // O must hold PV(j-1) before it is rescaled (and before PV(j) is issued,
             // which waits for this warpgroup's P).  Doing it after writing P keeps
             // PV(j-1) off the critical path.  With one S buffer S(j) was issued after
@@ -682,7 +648,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(C::B_PFULL + x));
-            if (r == 0) TRACE(2 + x, 4, j);
         }
         if (ok && !wait_warp(BAR(C::B_PVDONE + x), (nb - 1) & 1, abort_flag)) ok = false;
         if (!ok) {

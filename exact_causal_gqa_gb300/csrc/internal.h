@@ -112,4 +112,23 @@ int split_f32_tile_cols();
 cudaError_t launch_split_f32_tile(const SplitParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 
+// Multiprocessor count of the current device (cached per device); 152 (one
+// GB300) when no device is visible.
+int device_sm_count();
+
+// The split plan of a call: which kernel path, split geometry and workspace.  A
+// pure function of the call's sizes and the SM count (atlas_launch.sm_count, else
+// device_sm_count()).
+enum class Path { SplitBF16, SplitF32, SplitF32Tile, TensorCore };
+
+struct Plan {
+    Path path;
+    int chunk, n_chunks, col_tiles, G;
+    int tc_split, tiles_per_unit, tiles_per_head;
+    size_t acc_bytes, ml_offset, ws_bytes;
+};
+
+atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int32_t P,
+                       const atlas_launch *L, Plan *plan);
+
 }  // namespace atlas

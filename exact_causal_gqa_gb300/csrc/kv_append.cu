@@ -56,7 +56,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
 cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t stream) {
     const int64_t total = (int64_t)p.B * p.Hkv * p.max_new * (p.row_bytes / 16);
     int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    // a grid-stride loop over 16 CTAs of 256 threads per SM
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     kv_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
     return cudaGetLastError();

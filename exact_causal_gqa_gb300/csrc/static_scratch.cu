@@ -18,10 +18,14 @@
 // workspace.
 //
 // Nothing in the array has to start at zero: every partial the merge reads is
-// written by the split kernel of the same call.  The array is shared by all
-// calls on a device and keeps the last call's contents, so two calls whose
-// kernels overlap on the GPU (different streams, no ordering between them) race
-// on it and may return wrong results.
+// written by the split kernel of the same call.  That holds because the entry
+// point accepts ATLAS_PHASE_ALL only: a call spread over several launches
+// (ATLAS_PHASE_CHUNKS ... ATLAS_PHASE_MERGE) would leave its partials in the
+// shared array between launches, where any other call could overwrite them, so
+// such calls are refused.  The array is shared by all calls on a device and
+// keeps the last call's contents, so two calls whose kernels overlap on the GPU
+// (different streams, no ordering between them) race on it and may return wrong
+// results.
 #include "internal.h"
 
 #include <cuda_runtime.h>
@@ -61,12 +65,15 @@ extern "C" atlas_status atlas_attn_decode_static_scratch(
     const int32_t *seq_lens, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
     int32_t page_tokens, float scale, const atlas_launch *L) {
     if (!L) return ATLAS_ERR_INVALID_ARG;
-    const size_t need = atlas_attn_workspace_size(ATLAS_KIND_DECODE, n_q_heads, n_kv_heads,
-                                                  head_dim, page_tokens, L);
-    if (need == SIZE_MAX) return ATLAS_ERR_INVALID_ARG;
-    if (need > (size_t)ATLAS_STATIC_SCRATCH_BYTES) return ATLAS_ERR_WORKSPACE;
+    // The same plan atlas_attn_decode makes, with its status passed on unchanged.
+    atlas::Plan plan;
+    atlas_status st = atlas::make_plan(ATLAS_KIND_DECODE, n_q_heads, n_kv_heads, head_dim,
+                                       page_tokens, L, &plan);
+    if (st != ATLAS_OK) return st;
+    if (L->phase != ATLAS_PHASE_ALL) return ATLAS_ERR_UNSUPPORTED;
+    if (plan.ws_bytes > (size_t)ATLAS_STATIC_SCRATCH_BYTES) return ATLAS_ERR_WORKSPACE;
     void *scratch = nullptr;
-    atlas_status st = atlas::scratch_address(&scratch);
+    st = atlas::scratch_address(&scratch);
     if (st != ATLAS_OK) return st;
     atlas_launch local = *L;
     local.workspace = scratch;

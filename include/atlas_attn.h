@@ -138,6 +138,14 @@ typedef struct {
                                    NULL = every chunk.  Only page_table entries of those
                                    chunks' pages are read. */
     int32_t phase;             /* ATLAS_PHASE_ALL, _CHUNKS or _MERGE (below) */
+    int32_t sm_count;          /* SMs the automatic split plan fills; 0 = the multiprocessor
+                                  count of the current device (cached per device), or 152
+                                  (one GB300) when no device is visible, e.g. when sizing a
+                                  workspace on a host without a GPU.  A caller confined to
+                                  part of the GPU (a green context, an MPS share) passes its
+                                  own count.  The plan, and so the workspace size and the
+                                  bits of the result, is a pure function of the call's sizes
+                                  and this count. */
 } atlas_launch;
 
 /* atlas_launch.phase.  With a phase other than ALL the call always takes the
@@ -251,12 +259,16 @@ const char *atlas_attn_status_string(atlas_status status);
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Returns ATLAS_ERR_WORKSPACE when the call would need
- * more than ATLAS_STATIC_SCRATCH_BYTES of scratch (atlas_attn_workspace_size
- * with ATLAS_KIND_DECODE gives the need), ATLAS_ERR_CUDA if the address lookup
- * fails.  All calls on a device share the array: calls whose kernels may overlap
- * on the GPU (unordered streams) race on it.  Nothing in it needs clearing
- * between calls.
+ * any stream capture.  Returns the status atlas_attn_decode would return for
+ * invalid or unsupported arguments; ATLAS_ERR_UNSUPPORTED for L->phase other
+ * than ATLAS_PHASE_ALL (the partials of a call spread over several launches
+ * would sit in the shared array between launches); ATLAS_ERR_WORKSPACE when the
+ * call would need more than ATLAS_STATIC_SCRATCH_BYTES of scratch
+ * (atlas_attn_workspace_size with ATLAS_KIND_DECODE gives the need);
+ * ATLAS_ERR_CUDA if the address lookup fails.  All calls on a device share the
+ * array: calls whose kernels may overlap on the GPU (unordered streams) race on
+ * it.  Nothing in it needs clearing between calls, since each call's merge reads
+ * only partials its own split kernel wrote.
  */
 atlas_status atlas_attn_decode_static_scratch(const void *q, const void *k_pages,
                                               const void *v_pages, const int32_t *page_table,

@@ -188,3 +188,40 @@ def test_tensor_core_plan_sizes(lib):
     assert plan(2, 2, 32, 8, 8192, 8192, 64) == 0
     # a small prefill (64 tiles) is split, capped at its own length
     assert plan(2, 1, 8, 2, 1024, 1024, 64) == 1024
+
+
+def test_split_plan_follows_the_sm_count(lib):
+    """The automatic plan fills the SMs it is given (atlas_launch.sm_count): the split
+    targets scale with the count, and a count of 0 means the device's own (152, one
+    GB300, on a host without a GPU)."""
+    def plan(sms, batch=4, Hq=32, Hkv=8, ctx=32768, P=16, kind=0, q_len=1, **kw):
+        pages = ctx // P
+        return split_tokens(lib, kind=kind, Hq=Hq, Hkv=Hkv, P=P, batch=batch, q_len=q_len,
+                            max_pages_per_seq=pages, num_pages=batch * pages, sm_count=sms,
+                            **kw)
+
+    def expect(units, ctx, target, lo, hi):
+        chunk = -(-(-(-ctx * units // target)) // 64) * 64
+        return min(max(chunk, lo), hi)
+
+    # bf16 decode: SMs x 2 x 2 CTAs, 512..2560 keys
+    for sms in (152, 148, 132, 76, 20):
+        assert plan(sms) == expect(32, 32768, sms * 4, 512, 2560), sms
+    assert plan(0) == plan(152)
+    # fp32 ring (G = 4): SMs x 3 x 4 CTAs
+    f32 = dict(q_dtype=0, kv_dtype=0, out_dtype=0)
+    for sms in (152, 76):
+        assert plan(sms, batch=1, **f32) == expect(8, 32768, sms * 12, 64, 2560)
+    # tensor-core suffix: SMs x 3 CTAs, 1024..8192 keys in multiples of 128
+    for sms in (152, 40):
+        n = plan(sms, batch=1, Hq=32, Hkv=4, ctx=65536, P=32, kind=1, q_len=16)
+        tiles = 4
+        want = -(-(65536 * tiles) // (sms * 3))
+        want = min(max(-(-want // 128) * 128, 1024), 8192)
+        assert n == want, sms
+    # prefill writes its output directly at >= SMs x 2 query tiles (4096 here), so a
+    # part with 4096 / 2 + 1 SMs would split it
+    assert plan(152, batch=2, Hq=32, Hkv=8, ctx=8192, P=64, kind=2, q_len=8192) == 0
+    assert plan(2049, batch=2, Hq=32, Hkv=8, ctx=8192, P=64, kind=2, q_len=8192) > 0
+    # a negative count is an invalid argument
+    assert plan(-1) == -1

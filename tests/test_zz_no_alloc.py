@@ -36,9 +36,10 @@ def static_fn():
     return fn
 
 
-def call_static(prob, out):
+def call_static(prob, out, phase=atlas.PHASE_ALL):
     stream = torch.cuda.current_stream().cuda_stream
-    L = atlas._launch(prob.q, prob.k_pages, prob.page_table, out.dtype, out=out, stream=stream)
+    L = atlas._launch(prob.q, prob.k_pages, prob.page_table, out.dtype, out=out, stream=stream,
+                      phase=phase)
     return static_fn()(prob.q.data_ptr(), prob.k_pages.data_ptr(), prob.v_pages.data_ptr(),
                        prob.page_table.data_ptr(), prob.seq_lens.data_ptr(), prob.n_q_heads,
                        prob.n_kv_heads, prob.head_dim, prob.page_tokens, prob.scale,
@@ -69,6 +70,7 @@ def test_static_scratch_decode_matches_decode_on_two_calls_in_a_row():
         assert call_static(prob, out) == 0
         ref = atlas.run(prob, out_dtype=dtype)
         torch.cuda.synchronize()
+        assert torch.equal(out, ref)
         assert_close(out, ref)
 
 
@@ -85,3 +87,12 @@ def test_static_scratch_refuses_calls_beyond_its_size():
     assert need > STATIC_BYTES
     out = torch.empty_like(q)
     assert call_static(prob, out) == 3  # ATLAS_ERR_WORKSPACE, nothing launched
+
+
+def test_static_scratch_refuses_calls_spread_over_launches():
+    # The partials of a chunked call would sit in the shared array between its
+    # launches, where another call could overwrite them: only whole calls run here.
+    prob = inputs.make("decode", 2, 8, 2, 128, 16, [300, 41], seed=23).to("cuda")
+    out = torch.empty(prob.q.shape, dtype=torch.bfloat16, device="cuda")
+    assert call_static(prob, out, phase=atlas.PHASE_CHUNKS) == 2  # ATLAS_ERR_UNSUPPORTED
+    assert call_static(prob, out, phase=atlas.PHASE_MERGE) == 2
