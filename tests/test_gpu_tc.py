@@ -46,6 +46,28 @@ def test_suffix_parity(B, Hq, Hkv, P, SQ, lens, split):
     check(prob, split=split)
 
 
+D64 = [
+    # (kind, B, Hq, Hkv, P, q_len, lens)
+    ("suffix", 1, 8, 2, 16, 16, (256,)),        # the CPUAttn example: q (1,8,16,64), k/v (1,2,256,64)
+    ("suffix", 3, 32, 4, 32, 16, (16, 300, 1000)),
+    ("suffix", 2, 12, 4, 8, 8, (33, 2000)),
+    ("prefill", 1, 4, 1, 64, 128, None),
+    ("prefill", 2, 8, 2, 16, 300, None),
+    ("prefill", 1, 32, 8, 64, 200, None),
+]
+
+
+@pytest.mark.parametrize("kind,B,Hq,Hkv,P,q_len,lens", D64)
+@pytest.mark.parametrize("mode", ["auto", "split256", "direct"])
+def test_head_dim_64_parity(kind, B, Hq, Hkv, P, q_len, lens, mode):
+    """bf16 head_dim 64 with many query rows per kv head (suffix and prefill)."""
+    lens = list(lens) if lens else [q_len] * B
+    prob = inputs.make(kind, B, Hq, Hkv, 64, P, lens, q_len=q_len, seed=64 + B + Hq + P)
+    split = 256 if mode == "split256" else 0
+    flags = atlas.DEBUG_TC_DIRECT if mode == "direct" else 0
+    check(prob, split=split, flags=flags)
+
+
 PREFILL = [
     # (B, Hq, Hkv, P, S)
     (1, 4, 1, 64, 128),
@@ -121,29 +143,38 @@ def sampled(prob, rows, out32, out16):
     assert torch.isfinite(out32).all()
 
 
-def test_config4_suffix_full_size_sampled_rows():
+def test_config4_suffix_full_size_every_row():
+    """Suffix queries at full size (16 sequences x 32 heads x 16 rows, contexts up to
+    64K keys), in bench.py's launch configuration: every output row."""
     prob = inputs.make_config(4)
     dev = prob.to(DEV)
     out16 = run_gpu(dev)
     out32 = run_gpu(dev, out_dtype=torch.float32)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(4)
-    rows = np.unique(np.concatenate([rng.choice(flat_rows(prob), 96, replace=False),
-                                     [0, 15, flat_rows(prob) - 1]]))
-    sampled(prob, rows, out32, out16)
+    ref = oracle_rows(prob)
+    assert_parity(prob, out32, ref, "f32 out")
+    assert_parity(prob, out16, ref, "bf16 out")
+    assert torch.equal(out16, out32.to(torch.bfloat16))
 
 
-def test_config5_prefill_full_size_sampled_rows():
+def test_config5_prefill_full_size_whole_group_and_samples():
+    """Causal prefill at full size (2 x 8192 rows, 32 / 8 heads): every row of one
+    whole (sequence, kv head) group -- all its G q heads, all 8192 positions -- plus a
+    spread of rows over the other groups, including the first rows of tiles."""
     prob = inputs.make_config(5)
     dev = prob.to(DEV)
     out16 = run_gpu(dev)
     out32 = run_gpu(dev, out_dtype=torch.float32)
     torch.cuda.synchronize()
     S, H = prob.q_len, prob.n_q_heads
+    G = H // prob.n_kv_heads
+    b, g = 1, 5
+    group = [(b * H + h) * S + i for h in range(g * G, (g + 1) * G) for i in range(S)]
     rng = np.random.default_rng(5)
-    early = [(b * H + h) * S + i for b in range(2) for h in (0, 13, 31)
+    early = [(bb * H + h) * S + i for bb in range(2) for h in (0, 13, 31)
              for i in (0, 1, 2, 63, 127, 128, 511, 512, 4095, S - 1)]
-    rows = np.unique(np.concatenate([rng.choice(flat_rows(prob), 64, replace=False), early]))
+    rows = np.unique(np.concatenate([group, early,
+                                     rng.choice(flat_rows(prob), 256, replace=False)]))
     sampled(prob, rows, out32, out16)
 
 
