@@ -413,7 +413,7 @@ def measure(args, index, world, rank, local, e2e=True, cpu_budget=12.0):
         achieved = flops / (main_avg * 1e-3) / 1e12
         peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
         bound = "tensor"
-    tc_path = prob.dtype == "bf16" and prob.head_dim == 128 and \
+    tc_path = prob.dtype == "bf16" and \
         prob.q_len * (prob.n_q_heads // prob.n_kv_heads) > 16
     f32_tile = prob.dtype == "f32" and \
         prob.q_len * (prob.n_q_heads // prob.n_kv_heads) >= F32_TILE_MIN_COLS

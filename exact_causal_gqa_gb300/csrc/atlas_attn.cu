@@ -134,7 +134,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     plan->G = G;
     plan->tc_split = 0;
     plan->tiles_per_unit = plan->tiles_per_head = 0;
-    if (L->kv_dtype == ATLAS_BF16 && D == 128 && (int64_t)G * L->q_len > 16) {
+    if (L->kv_dtype == ATLAS_BF16 && (int64_t)G * L->q_len > 16) {
         // Many query rows per (sequence, kv head): 128-row tiles on tcgen05.
         plan->path = Path::TensorCore;
         const int64_t tiles_per_unit = ((int64_t)G * L->q_len + 127) / 128;
@@ -334,6 +334,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         tp.Hq = Hq;
         tp.Hkv = Hkv;
         tp.G = plan.G;
+        tp.D = D;
         tp.P = P;
         tp.q_len = L->q_len;
         tp.max_pages = L->max_pages_per_seq;

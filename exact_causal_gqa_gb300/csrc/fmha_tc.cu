@@ -17,8 +17,9 @@
 //   warp 0    TMA producer: the Q tiles once, then K and V blocks gathered page
 //             by page through the page table into a KV_STAGES-deep ring.
 //   warp 1    allocates TMEM; one lane issues the MMAs:
-//               S  = Q K^T  (M=128, N=128, K=128; A and B from smem)  -> TMEM
-//               O += P V    (M=128, N=128, K=128; A = P from TMEM, B = V from smem)
+//               S  = Q K^T  (M=128, N=128, K=D; A and B from smem)  -> TMEM
+//               O += P V    (M=128, N=D, K=128; A = P from TMEM, B = V from smem)
+//             for head_dim D = 64 or 128 (one or two 64-element slabs per row).
 //   warp 2    zeroes V rows past the last key of the final block (they may be
 //             NaN-poisoned or stale, and 0 * NaN would reach O).
 //   warps 4+  one softmax warpgroup per tile, one thread per query row: read the
@@ -39,8 +40,7 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per block
-constexpr int kTileBytes = 128 * 128 * 2;  // a 128 x 128 bf16 tile (Q, K or V)
-constexpr int kSlab = 128 * 128;           // one 64-column slab of such a tile
+constexpr int kSlab = 128 * 128;  // one 64-element slab of a 128-row bf16 tile (128-byte rows)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows 256x
 // A block takes P as bf16 hi + lo when, for some row of the tile, its largest weight
@@ -51,9 +51,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max
 // the log domain against log2(w / (1 - w)) = log2(1/19).
 constexpr float kLog2HiLo = -4.2479275f;
 
-template <int NT>
+template <int NT, int D>
 struct Cfg {
-    static constexpr int kStages = NT == 2 ? 2 : 3;  // K/V ring depth
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static constexpr int kSlabs = D / 64;             // 64-element slabs per row
+    static constexpr int kTileBytes = 128 * D * 2;    // a 128-row bf16 tile (Q, K or V)
+    // K/V ring depth: the same bytes in flight for either head_dim
+    static constexpr int kStages = (NT == 2 ? 2 : 3) * (128 / D);
     static constexpr int kSB = NT == 2 ? 1 : 2;      // S buffers per tile
     // warps 0-2: producer, MMA issuer, tail fix-up (warp 3 idle); then NT softmax
     // warpgroups.  Each SMSP holds 16K registers and 3 of the 12 warps (NT = 2):
@@ -104,27 +108,29 @@ __device__ __forceinline__ int64_t tile_row(const TcParams &p, int b, int hkv, i
 }
 
 // NaN for row f of (b, hkv) in direct mode.
+template <int D>
 __device__ void nan_row(const TcParams &p, int b, int hkv, int f) {
     const int64_t row = tile_row(p, b, hkv, f);
     const float nan = __int_as_float(0x7fc00000);
     if (p.out_bf16) {
         uint4 v;
         v.x = v.y = v.z = v.w = 0x7fc07fc0u;
-        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + row * 128);
-        for (int k = 0; k < 16; ++k) o[k] = v;
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + row * D);
+        for (int k = 0; k < D / 8; ++k) o[k] = v;
     } else {
-        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * 128);
-        for (int k = 0; k < 32; ++k) o[k] = make_float4(nan, nan, nan, nan);
+        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * D);
+        for (int k = 0; k < D / 4; ++k) o[k] = make_float4(nan, nan, nan, nan);
     }
     if (p.lse) p.lse[row] = nan;
 }
 
-template <int NT>
-__global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
+template <int NT, int D>
+__global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const TcParams p) {
-    using C = Cfg<NT>;
+    using C = Cfg<NT, D>;
     constexpr int S = C::kStages, SB = C::kSB;
+    constexpr int kTileBytes = C::kTileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         const int rows_valid = (qn >= 0 && qn <= p.q_len) ? qn : p.q_len;
         if (!p.split && threadIdx.x < NT * BM) {
             const int f = (t0 + (int)(threadIdx.x / BM) * tstep) * BM + threadIdx.x % BM;
-            if (f < rows_unit && f % p.q_len < rows_valid) nan_row(p, b, hkv, f);
+            if (f < rows_unit && f % p.q_len < rows_valid) nan_row<D>(p, b, hkv, f);
         }
         return;  // split mode: the merge writes NaN rows for this sequence
     }
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 const int f = (t0 + (int)(threadIdx.x / BM) * tstep) * BM + threadIdx.x % BM;
                 if (f < rows_unit && f % p.q_len < qn) {
                     if (!p.split) {
-                        nan_row(p, b, hkv, f);
+                        nan_row<D>(p, b, hkv, f);
                     } else {
                         float *ml = p.ws_ml + (tile_row(p, b, hkv, f) * p.n_chunks + c) * 2;
                         ml[0] = ml[1] = __int_as_float(0x7fc00000);
@@ -266,8 +272,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             mbar_arrive_expect_tx(BAR(C::B_Q), NT * kTileBytes);
             for (int x = 0; x < NT; ++x) {
                 const int qrow = (int)tile_row(p, b, hkv, (t0 + x * tstep) * BM);
-                tma_load_2d(sb + C::OFF_Q + x * kTileBytes, &tmQ, 0, qrow, BAR(C::B_Q));
-                tma_load_2d(sb + C::OFF_Q + x * kTileBytes + kSlab, &tmQ, 64, qrow, BAR(C::B_Q));
+#pragma unroll
+                for (int sl = 0; sl < C::kSlabs; ++sl)
+                    tma_load_2d(sb + C::OFF_Q + x * kTileBytes + sl * kSlab, &tmQ, 64 * sl, qrow,
+                                BAR(C::B_Q));
             }
         }
         PageIdCache pages{p.page_table + (int64_t)b * p.max_pages, (kv_end - 1) / p.P};
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const int kb = kv_begin + j * BN;
             const int ke = min(kb + BN, kv_end);
             const int nbox = (ke - kb + BR - 1) / BR;
-            const uint32_t bytes = (uint32_t)(nbox * BR * 128 * 2);
+            const uint32_t bytes = (uint32_t)(nbox * BR * 128 * C::kSlabs);
             // y coordinate of box bx of this block (lane bx holds it; nbox <= 16)
             int my_y = 0;
             for (int bx = 0; bx < nbox; ++bx) {
@@ -298,8 +306,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     const uint32_t dst = sb + (kv == 0 ? C::OFF_K : C::OFF_V) + s * kTileBytes;
                     if (lane == 0) mbar_arrive_expect_tx(BAR(full), bytes);
                     __syncwarp((1u << nbox) - 1u);
-                    tma_load_2d(dst + lane * BR * 128, map, 0, my_y, BAR(full));
-                    tma_load_2d(dst + kSlab + lane * BR * 128, map, 64, my_y, BAR(full));
+#pragma unroll
+                    for (int sl = 0; sl < C::kSlabs; ++sl)
+                        tma_load_2d(dst + sl * kSlab + lane * BR * 128, map, 64 * sl, my_y,
+                                    BAR(full));
                 }
                 __syncwarp();
                 if (kv == 0) issued_k = j + 1;
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(128, 128, false, p.negate_scores != 0);
-            constexpr uint32_t idPV = idesc_bf16_f32(128, 128, true);
+            constexpr uint32_t idPV = idesc_bf16_f32(128, D, true);
             bool ok = mbar_wait_bounded(BAR(C::B_Q), 0, abort_flag, kWaitLimitNs);
             tc_fence_after();
             // S_x(j) = Q_x K_j^T into S buffer j % SB of tile x.  Tile 0 waits for
@@ -339,7 +349,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 const uint64_t kd = sdesc_sw128(sb + C::OFF_K + s * kTileBytes, 16, 1024);
                 const uint64_t qd = sdesc_sw128(sb + C::OFF_Q + x * kTileBytes, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
                     umma_bf16(tmem + C::s_col(x, j % SB), qd + off, kd + off, idS, kk > 0);
                 }
@@ -429,8 +439,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const int s = (nb - 1) % S;
             if (wait_warp(BAR(C::B_TAIL_READY), 0, abort_flag)) {
                 const uint32_t vbase = sb + C::OFF_V + s * kTileBytes;
-                for (int idx = lane; idx < (BN - tail_first) * 16; idx += 32) {
-                    const int row = tail_first + idx / 16, q = idx % 16;
+                constexpr int kChunks = 8 * C::kSlabs;  // 16-byte chunks per V row
+                for (int idx = lane; idx < (BN - tail_first) * kChunks; idx += 32) {
+                    const int row = tail_first + idx / kChunks, q = idx % kChunks;
                     st_shared_v4(vbase + (q / 8) * kSlab + row * 128 + (q % 8) * 16, 0u, 0u, 0u,
                                  0u);
                 }
@@ -636,7 +647,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             tc_fence_after();
             if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
                     tmem_ld32(to + cc * 32, o);
                     tmem_wait_ld();
@@ -671,13 +682,13 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const float inv = osc / l;
             const int64_t slot = row * p.n_chunks + c;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
                 tmem_ld32(to + cc * 32, o);
                 tmem_wait_ld();
                 if (!valid) continue;
                 if (p.split) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + slot * 128 + cc * 32);
+                    float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + slot * D + cc * 32);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
@@ -685,7 +696,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                                              __uint_as_float(o[4 * k + 3]));
                 } else if (p.out_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                           row * 128 + cc * 32);
+                                                           row * D + cc * 32);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint4 v;
@@ -701,7 +712,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
-                                                             row * 128 + cc * 32);
+                                                             row * D + cc * 32);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv,
@@ -723,7 +734,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 const int64_t slot = tile_row(p, b, hkv, f) * p.n_chunks + c;
                 p.ws_ml[slot * 2] = p.ws_ml[slot * 2 + 1] = __int_as_float(0x7fc00000);
             } else {
-                nan_row(p, b, hkv, f);
+                nan_row<D>(p, b, hkv, f);
             }
         }
     }
@@ -738,23 +749,23 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
 #undef BAR
 }
 
-template <int NT>
+template <int NT, int D>
 cudaError_t launch_instance(const TcParams &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                             const CUtensorMap &tmV, cudaStream_t stream) {
-    using C = Cfg<NT>;
+    using C = Cfg<NT, D>;
     static int configured[64] = {0};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 64 && !configured[dev]) {
-        err = cudaFuncSetAttribute(fmha_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   C::kSmem);
+        err = cudaFuncSetAttribute(fmha_tc_kernel<NT, D>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (err != cudaSuccess) return err;
         configured[dev] = 1;
     }
     const int tiles = p.B * p.Hkv * p.tiles_per_unit;
     dim3 grid = p.split ? dim3(p.n_chunks, tiles, 1) : dim3(tiles / NT, 1, 1);
-    fmha_tc_kernel<NT><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, p);
+    fmha_tc_kernel<NT, D><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 
@@ -765,8 +776,11 @@ cudaError_t launch_fmha_tc(const TcParams &p, const CUtensorMap &tmQ, const CUte
     // Two tiles per CTA when two q heads of a group can share every K/V block:
     // direct output, an even group, prompt rows in whole tiles.
     const bool pair = !p.split && p.tiles_per_head > 0 && p.G % 2 == 0;
-    return pair ? launch_instance<2>(p, tmQ, tmK, tmV, stream)
-                : launch_instance<1>(p, tmQ, tmK, tmV, stream);
+    if (p.D == 64)
+        return pair ? launch_instance<2, 64>(p, tmQ, tmK, tmV, stream)
+                    : launch_instance<1, 64>(p, tmQ, tmK, tmV, stream);
+    return pair ? launch_instance<2, 128>(p, tmQ, tmK, tmV, stream)
+                : launch_instance<1, 128>(p, tmQ, tmK, tmV, stream);
 }
 
 }  // namespace atlas

@@ -58,13 +58,13 @@ struct MergeParams {
 };
 
 // Tensor-core (tcgen05 / TMEM) path for many query rows per (sequence, kv head):
-// 128-row query tiles x 128-key blocks, head_dim 128, bf16.  Either writes the
+// 128-row query tiles x 128-key blocks, head_dim 64 or 128, bf16.  Either writes the
 // normalised output directly (one CTA per tile, all its keys) or, when there are
 // too few tiles to fill the GPU, split partials in the SplitParams layout.
 struct TcParams {
     const int32_t *page_table;
     const int32_t *seq_lens;
-    int32_t B, Hq, Hkv, G, P, q_len, max_pages, num_pages;
+    int32_t B, Hq, Hkv, G, D, P, q_len, max_pages, num_pages;
     int32_t tiles_per_unit;   // ceil(G * q_len / 128)
     int32_t tiles_per_head;   // q_len / 128 when q_len % 128 == 0 (heavy-first order), else 0
     int32_t split;            // 1: write split partials; 0: write the output
