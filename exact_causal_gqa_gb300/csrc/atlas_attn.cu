@@ -68,6 +68,16 @@ constexpr float kHiLoScale = 1.25f;
 constexpr int kF32TileMinCols = 64;
 int64_t f32_tile_plan_ctas(int sms) { return (int64_t)sms * 8; }
 
+// A bf16 decode-like call whose whole context per (sequence, kv head) holds at most
+// this many K/V bytes runs as one split per (sequence, kv head, column tile) that
+// writes its output directly: at that size the merge launch (a few microseconds)
+// costs more than the parallelism the splits add.
+constexpr int64_t kDirectMaxBytes = 256 * 1024;
+// An fp32 ring-kernel call whose automatic plan has at most this many splits runs
+// them as one thread-block cluster per (sequence, kv head, column tile), merged in
+// distributed shared memory (the portable cluster size limit).
+constexpr int kClusterMaxSplits = 8;
+
 // One GB300: the count the plan assumes when no device is visible.
 constexpr int kDefaultSms = 152;
 
@@ -132,6 +142,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
 
     const int G = Hq / Hkv;
     plan->G = G;
+    plan->direct = plan->cluster = 0;
     plan->tc_split = 0;
     plan->tiles_per_unit = plan->tiles_per_head = 0;
     if (L->kv_dtype == ATLAS_BF16 && (int64_t)G * L->q_len > 16) {
@@ -180,6 +191,15 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     if ((int64_t)Hkv * plan->col_tiles > 65535 || L->batch > 65535) return ATLAS_ERR_UNSUPPORTED;
 
     int64_t chunk = L->split_tokens;
+    const int64_t unit_bytes = max_ctx * 2 * D * (L->kv_dtype == ATLAS_BF16 ? 2 : 4);
+    const bool whole_call = chunk == 0 && L->phase == ATLAS_PHASE_ALL && !L->chunk_range;
+    if (whole_call && plan->path == Path::SplitBF16 && unit_bytes <= kDirectMaxBytes) {
+        plan->direct = 1;
+        plan->chunk = (int)round_up(max_ctx, kSplitBlockTokens);
+        plan->n_chunks = 1;
+        plan->acc_bytes = plan->ml_offset = plan->ws_bytes = 0;
+        return ATLAS_OK;
+    }
     if (chunk == 0 && plan->path == Path::SplitF32Tile) {
         const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
         const int64_t target = f32_tile_plan_ctas(sms);
@@ -199,6 +219,11 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     if (chunk > max_ctx) chunk = round_up(max_ctx, kSplitBlockTokens);
     plan->chunk = (int)chunk;
     plan->n_chunks = (int)((max_ctx + chunk - 1) / chunk);
+    if (whole_call && plan->path == Path::SplitF32 && plan->n_chunks <= kClusterMaxSplits) {
+        plan->cluster = 1;
+        plan->acc_bytes = plan->ml_offset = plan->ws_bytes = 0;
+        return ATLAS_OK;
+    }
 
     const int64_t rows = (int64_t)L->batch * Hq * L->q_len;
     plan->acc_bytes = (size_t)rows * plan->n_chunks * D * sizeof(float);
@@ -310,6 +335,12 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     sp.ws_ml = reinterpret_cast<float *>(static_cast<char *>(L->workspace) + plan.ml_offset);
     sp.status = L->status_word;
     sp.debug_flags = L->debug_flags;
+    sp.direct = plan.direct;
+    sp.cluster = plan.cluster;
+    sp.out = L->out;
+    sp.out_bf16 = L->out_dtype == ATLAS_BF16;
+    sp.lse = L->lse;
+    sp.sinks = L->sinks;
 
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     if (L->events)
@@ -384,7 +415,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     if (err != cudaSuccess) return ATLAS_ERR_CUDA;
     if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
     }
-    if (L->phase == ATLAS_PHASE_CHUNKS) {
+    if (L->phase == ATLAS_PHASE_CHUNKS || plan.direct || plan.cluster) {
         if (ev[2] && cudaEventRecord(ev[2], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
         return ATLAS_OK;
     }
@@ -495,7 +526,7 @@ int32_t atlas_attn_split_tokens(atlas_kind kind, int32_t n_q_heads, int32_t n_kv
     atlas::Plan plan;
     if (atlas::make_plan(kind, n_q_heads, n_kv_heads, head_dim, page_tokens, L, &plan) != ATLAS_OK)
         return -1;
-    return plan.n_chunks > 0 ? plan.chunk : 0;
+    return plan.n_chunks > 0 && !plan.direct && !plan.cluster ? plan.chunk : 0;
 }
 
 const char *atlas_attn_status_string(atlas_status status) {

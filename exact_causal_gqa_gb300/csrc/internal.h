@@ -42,6 +42,17 @@ struct SplitParams {
     float *ws_ml;               // [B*Hq*q_len][n_chunks][2]   (m in log2 units, l)
     uint32_t *status;           // may be null
     uint32_t debug_flags;
+    // Direct mode (bf16): one split covers the whole context; the split kernel
+    // writes the output rows itself (no workspace, no merge).
+    int32_t direct;
+    // Cluster mode (f32): the n_chunks (<= 8) splits of one (sequence, kv head,
+    // column tile) run as one thread-block cluster and merge through distributed
+    // shared memory; rank 0 writes the output rows (no workspace, no merge launch).
+    int32_t cluster;
+    void *out;
+    int32_t out_bf16;
+    float *lse;
+    const float *sinks;         // [Hq] natural-log logits or null (direct mode only)
 };
 
 struct MergeParams {
@@ -123,6 +134,8 @@ enum class Path { SplitBF16, SplitF32, SplitF32Tile, TensorCore };
 
 struct Plan {
     Path path;
+    int direct;   // bf16 split kernel: one split, output written directly
+    int cluster;  // f32 split kernel: splits merged inside one thread-block cluster
     int chunk, n_chunks, col_tiles, G;
     int tc_split, tiles_per_unit, tiles_per_head;
     size_t acc_bytes, ml_offset, ws_bytes;

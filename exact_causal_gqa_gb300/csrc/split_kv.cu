@@ -65,14 +65,36 @@ __device__ __forceinline__ float score_log2(const SplitParams &p, float raw) {
                                 : raw * p.scale_log2;
 }
 
+// Direct mode (p.direct): NaN for every row of columns [col0, col0 + ncols) of
+// (b, hkv) that is a query (all of them when `all_rows`, as for a bad seq_len).
+__device__ void direct_nan_rows(const SplitParams &p, int b, int hkv, int col0, int ncols,
+                                int qn, bool all_rows) {
+    const float nan = __int_as_float(0x7fc00000);
+    for (int idx = threadIdx.x; idx < ncols * p.D; idx += blockDim.x) {
+        const int c = idx / p.D, d = idx % p.D;
+        if (!all_rows && (col0 + c) % p.q_len >= qn) continue;
+        const int64_t row = column_row(p, b, hkv, col0 + c);
+        if (p.out_bf16)
+            static_cast<__nv_bfloat16 *>(p.out)[row * p.D + d] = __float2bfloat16_rn(nan);
+        else
+            static_cast<float *>(p.out)[row * p.D + d] = nan;
+        if (d == 0 && p.lse) p.lse[row] = nan;
+    }
+}
+
 // Shared prologue: decides whether this CTA has work.  Returns false when the
 // CTA must exit (nothing visible, or an error that has been recorded).
 // Returns L shifted to L - qn + q_len: with it, row i (< qn) of a ragged sequence
 // sits at position L_shifted - q_len + i = seq_len - qn + i, as in a full batch.
 // Columns with row index >= qn are padding (qn out).
+// Why split_prologue found no work for the CTA.
+constexpr int kNoWork = 1;   // nothing of this split is visible to its columns
+constexpr int kBadPage = 2;  // a page id outside the pool (recorded)
+constexpr int kBadLen = 3;   // the sequence's seq_len / q_lens are invalid (recorded)
+
 template <int NCOLS>
 __device__ bool split_prologue(const SplitParams &p, int ct, int &L, int &kv_begin, int &kv_end,
-                               int &col0, int &ncols, int &qn) {
+                               int &col0, int &ncols, int &qn, int &why) {
     const int b = blockIdx.z;
     const int hkv = blockIdx.y / p.col_tiles;
     // A pass of a call spread over several launches computes some splits only.
@@ -81,13 +103,18 @@ __device__ bool split_prologue(const SplitParams &p, int ct, int &L, int &kv_beg
         return false;
     L = p.seq_lens[b];
     qn = p.q_lens ? p.q_lens[b] : p.q_len;
-    if (seq_len_bad(p, L, qn)) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) record(p.status, ATLAS_DEV_BAD_SEQLEN);
-        return false;  // the merge writes NaN rows for this sequence
-    }
-    L = L - qn + p.q_len;
     col0 = ct * NCOLS;
     ncols = min(NCOLS, p.G * p.q_len - col0);
+    why = kNoWork;
+    if (seq_len_bad(p, L, qn)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) record(p.status, ATLAS_DEV_BAD_SEQLEN);
+        // split mode: the merge writes NaN rows for this sequence; cluster mode:
+        // the cluster's rank 0 does
+        if (p.direct) direct_nan_rows(p, b, hkv, col0, ncols, qn, true);
+        why = kBadLen;
+        return false;
+    }
+    L = L - qn + p.q_len;
     int i_max = -1, i_min = p.q_len;
     for (int c = 0; c < ncols; ++c) {
         const int i = (col0 + c) % p.q_len;
@@ -112,6 +139,12 @@ __device__ bool split_prologue(const SplitParams &p, int ct, int &L, int &kv_beg
     }
     if (__syncthreads_or(bad)) {
         if (threadIdx.x == 0) record(p.status, ATLAS_DEV_BAD_PAGE);
+        why = kBadPage;
+        if (p.direct) {
+            direct_nan_rows(p, b, hkv, col0, ncols, qn, false);
+            return false;
+        }
+        if (p.cluster) return false;  // a NaN state for this split, merged in the cluster
         for (int c = threadIdx.x; c < ncols; c += blockDim.x) {
             float *ml = p.ws_ml + (column_row(p, b, hkv, col0 + c) * p.n_chunks + blockIdx.x) * 2;
             ml[0] = __int_as_float(0x7fc00000);
@@ -124,16 +157,32 @@ __device__ bool split_prologue(const SplitParams &p, int ct, int &L, int &kv_beg
 
 // Combine the per-warp states held in shared memory and write this split's
 // partial (m, l, acc) for every valid column.  cm/cl: [W][NCOLS]; cacc: [W][NCOLS][D].
+// Direct mode (one split covers the whole context): write the output row itself
+// with the merge's arithmetic on that single state (the sink, if any, as one more
+// state m = sink log2 e, l = 1, acc = 0), so the bits equal split + merge of it;
+// padding rows of a ragged batch are not written.
+// Cluster mode: the state (acc[D], m, l) of each column goes to `part` in this
+// CTA's shared memory ([NCOLS][D + 2]) for the cluster merge.
 template <int W, int NCOLS, int D>
 __device__ void write_partials(const SplitParams &p, const float *cm, const float *cl,
-                               const float *cacc, int col0, int ncols, bool failed) {
+                               const float *cacc, int col0, int ncols, int qn, bool failed,
+                               float *part = nullptr) {
     const int b = blockIdx.z;
     const int hkv = blockIdx.y / p.col_tiles;
+    if (p.direct && failed) {
+        direct_nan_rows(p, b, hkv, col0, ncols, qn, false);
+        return;
+    }
     for (int idx = threadIdx.x; idx < NCOLS * D; idx += blockDim.x) {
         const int c = idx / D, d = idx % D;
         if (c >= ncols) continue;
         const int64_t row = column_row(p, b, hkv, col0 + c);
         const int64_t slot = row * p.n_chunks + blockIdx.x;
+        if (part && failed) {
+            part[c * (D + 2) + d] = __int_as_float(0x7fc00000);
+            if (d == 0) part[c * (D + 2) + D] = part[c * (D + 2) + D + 1] = __int_as_float(0x7fc00000);
+            continue;
+        }
         if (failed) {
             if (d == 0) {
                 p.ws_ml[slot * 2] = __int_as_float(0x7fc00000);
@@ -152,6 +201,35 @@ __device__ void write_partials(const SplitParams &p, const float *cm, const floa
                 a += f * cacc[(w * NCOLS + c) * D + d];
                 l += f * cl[w * NCOLS + c];
             }
+        }
+        if (part) {
+            part[c * (D + 2) + d] = a;
+            if (d == 0) {
+                part[c * (D + 2) + D] = M;
+                part[c * (D + 2) + D + 1] = l;
+            }
+            continue;
+        }
+        if (p.direct) {
+            if ((col0 + c) % p.q_len >= qn) continue;  // padding row: not written
+            const float sink2 = p.sinks ? p.sinks[(row / p.q_len) % p.Hq] * kLog2e : -INFINITY;
+            float M2 = sink2;
+            if (l > 0.f) M2 = fmaxf(M2, M);
+            float o, lse;
+            if (isnan(l) || isnan(M) || isnan(sink2) || M2 == -INFINITY) {
+                o = lse = __int_as_float(0x7fc00000);
+            } else {
+                const float w = l > 0.f ? ex2(M - M2) : 0.f;
+                const float lsum = fmaf(w, l, p.sinks ? ex2(sink2 - M2) : 0.f);
+                o = fmaf(w, a, 0.f) / lsum;
+                lse = kLn2 * (M2 + log2f(lsum));
+            }
+            if (p.out_bf16)
+                static_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(o);
+            else
+                static_cast<float *>(p.out)[row * D + d] = o;
+            if (d == 0 && p.lse) p.lse[row] = lse;
+            continue;
         }
         p.ws_acc[slot * D + d] = a;
         if (d == 0) {
@@ -208,9 +286,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
     const uint32_t empty0 = full0 + STAGES * 8;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lay::kFlags);
 
-    int L, kv_begin, kv_end, col0, ncols, qn;
+    int L, kv_begin, kv_end, col0, ncols, qn, why;
     if (!split_prologue<NCOLS>(p, blockIdx.y % p.col_tiles, L, kv_begin, kv_end, col0, ncols,
-                               qn))
+                               qn, why))
         return;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -489,7 +567,110 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
             }
     }
     __syncthreads();
-    write_partials<kConsumerWarps, NCOLS, D>(p, cm, cl, cacc, col0, ncols, any_failed);
+    write_partials<kConsumerWarps, NCOLS, D>(p, cm, cl, cacc, col0, ncols, qn, any_failed);
+}
+
+// ---------------------------------------------------------------- cluster merge
+// Cluster mode: the n_chunks splits of one (sequence, kv head, column tile) are the
+// CTAs of one thread-block cluster (rank = split index).  Each leaves its partial
+// state in its own shared memory; the CTAs then read them through distributed
+// shared memory and apply the structured merge (CPUAttn README, "Operator model")
+// to a share of the output elements each, with the merge kernel's arithmetic in
+// split order, so the bits equal split + merge.
+// No workspace, no second launch.  Every CTA reaches both cluster barriers on every
+// path (no early exit in this mode), and the loops before them are bounded.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 32-bit load from the shared memory of CTA `rank` of this cluster, at the offset
+// that `local` (a shared-memory address of this CTA) has in its own.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+template <int NCOLS, int D>
+__device__ void cluster_merge(const SplitParams &p, const float *part, int col0, int ncols,
+                              int qn, bool bad_len) {
+    constexpr int kMaxSplits = 8;  // the portable cluster size
+    __syncthreads();
+    cluster_barrier();  // every split's state is in its CTA's shared memory
+    {
+        // The output rows' elements are shared out over every CTA of the cluster;
+        // each element's loads from all splits are issued before any is used.
+        const int b = blockIdx.z;
+        const int hkv = blockIdx.y / p.col_tiles;
+        const int L = p.seq_lens[b];
+        const uint32_t base = smem_u32(part);
+        const int rank = (int)cluster_ctarank();
+        for (int idx = rank * (int)blockDim.x + (int)threadIdx.x; idx < ncols * D;
+             idx += p.n_chunks * (int)blockDim.x) {
+            const int c = idx / D, d = idx % D;
+            const int i = (col0 + c) % p.q_len;
+            if (!bad_len && i >= qn) continue;  // padding row: not written
+            const int64_t row = column_row(p, b, hkv, col0 + c);
+            float o = __int_as_float(0x7fc00000), lse = o;
+            if (!bad_len) {
+                const int visible = L - qn + i + 1;
+                // splits holding this row's keys: [first, nsplit)
+                const int first = p.window > 0 ? max(0, visible - p.window) / p.chunk : 0;
+                const int nsplit = min((visible + p.chunk - 1) / p.chunk, p.n_chunks);
+                const uint32_t am = base + (uint32_t)(c * (D + 2) + D) * 4u;
+                const uint32_t aa = base + (uint32_t)(c * (D + 2) + d) * 4u;
+                float m[kMaxSplits], l[kMaxSplits], a[kMaxSplits];
+#pragma unroll
+                for (int u = 0; u < kMaxSplits; ++u) {
+                    m[u] = l[u] = a[u] = 0.f;
+                    if (first + u < nsplit) {
+                        m[u] = ld_cluster_f32(am, first + u);
+                        l[u] = ld_cluster_f32(am + 4, first + u);
+                        a[u] = ld_cluster_f32(aa, first + u);
+                    }
+                }
+                const float sink2 =
+                    p.sinks ? p.sinks[(row / p.q_len) % p.Hq] * kLog2e : -INFINITY;
+                float M = sink2;
+                bool has_nan = isnan(sink2);
+#pragma unroll
+                for (int u = 0; u < kMaxSplits; ++u) {
+                    if (first + u >= nsplit) break;
+                    if (isnan(l[u]) || isnan(m[u])) has_nan = true;
+                    else if (l[u] > 0.f) M = fmaxf(M, m[u]);
+                }
+                if (!has_nan && M != -INFINITY) {
+                    float lsum = p.sinks ? ex2(sink2 - M) : 0.f, acc = 0.f;
+#pragma unroll
+                    for (int u = 0; u < kMaxSplits; ++u) {
+                        if (first + u >= nsplit) break;
+                        const float w = l[u] > 0.f ? ex2(m[u] - M) : 0.f;
+                        lsum = fmaf(w, l[u], lsum);
+                        acc = fmaf(w, a[u], acc);
+                    }
+                    o = acc / lsum;
+                    lse = kLn2 * (M + log2f(lsum));
+                }
+            }
+            if (p.out_bf16)
+                static_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(o);
+            else
+                static_cast<float *>(p.out)[row * D + d] = o;
+            if (d == 0 && p.lse) p.lse[row] = lse;
+        }
+    }
+    __syncthreads();
+    cluster_barrier();  // every CTA has read the states it needs before any exits
 }
 
 // ---------------------------------------------------------------- f32 path
@@ -503,13 +684,13 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 // P back from shared memory.  Keys past the split's end are zero-filled, never read.
 constexpr int kF32Keys = 8;
 
+// Warps per CTA of the split form: each warp holds ~17 KB of rings (D = 128), so
+// 4-warp CTAs three to an SM keep 12 warps resident where 8-warp CTAs fit one; the
+// kernel is latency-bound (dependent shuffles, exponentials and shared-memory round
+// trips per 8-key block), and 12 warps measured 25-31 % faster than 8.  16 columns
+// need ~205 registers a thread, more than three CTAs allow.
 template <int D, int NC>
 struct F32Layout {
-    // Warps per CTA and CTAs per SM: each warp holds ~17 KB of rings (D = 128), so
-    // 4-warp CTAs three to an SM keep 12 warps resident where 8-warp CTAs fit one;
-    // the kernel is latency-bound (dependent shuffles, exponentials and shared-memory
-    // round trips per 8-key block), and 12 warps measured 25-31 % faster than 8.
-    // 16 columns need ~205 registers a thread, more than three CTAs allow.
     static constexpr int W = NC == 16 ? 8 : 4;
     static constexpr int kMinCtas = NC == 16 ? 1 : 3;
     static constexpr int KS = D + 4;                      // padded row stride (floats)
@@ -517,6 +698,8 @@ struct F32Layout {
     static constexpr int kWarp = 4 * kBuf + kF32Keys * NC;  // K[2], V[2], P[key][col]
     static constexpr int kQ = NC * KS;
     static constexpr int kBytes = (kQ + W * kWarp) * 4;
+    // cluster mode only: this split's state per column, [NC][D + 2], after the rings
+    static constexpr int kPartBytes = NC * (D + 2) * 4;
     static_assert(2 * W * NC + W * NC * D <= W * kWarp, "combine scratch fits the rings");
 };
 
@@ -528,10 +711,20 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
     extern __shared__ __align__(16) float f32d_smem[];
     float *sQ = f32d_smem;
     float *sW = sQ + Lay::kQ;
+    float *part = sW + W * Lay::kWarp;  // cluster mode only
 
-    int L, kv_begin, kv_end, col0, ncols, qn;
-    if (!split_prologue<NC>(p, blockIdx.y % p.col_tiles, L, kv_begin, kv_end, col0, ncols, qn))
+    int L = 0, kv_begin = 0, kv_end = 0, col0 = 0, ncols = 0, qn = 0, why = 0;
+    const bool work = split_prologue<NC>(p, blockIdx.y % p.col_tiles, L, kv_begin, kv_end, col0,
+                                         ncols, qn, why);
+    if (!work && !p.cluster) return;
+    if (!work) {
+        // an empty state (m = -inf, l = 0, acc = 0), or NaN after a bad page id
+        const float nan = __int_as_float(0x7fc00000);
+        for (int idx = threadIdx.x; idx < NC * (D + 2); idx += W * 32)
+            part[idx] = why == kBadPage ? nan : (idx % (D + 2) == D ? -INFINITY : 0.f);
+        cluster_merge<NC, D>(p, part, col0, ncols, qn, why == kBadLen);
         return;
+    }
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int b = blockIdx.z;
     const int hkv = blockIdx.y / p.col_tiles;
@@ -717,7 +910,12 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
 #pragma unroll
         for (int e = 0; e < DPL; ++e) cacc[(warp * NC + c) * D + lane * DPL + e] = acc[c][e];
     __syncthreads();
-    write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, false);
+    if (p.cluster) {
+        write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, qn, false, part);
+        cluster_merge<NC, D>(p, part, col0, ncols, qn, false);
+        return;
+    }
+    write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, qn, false);
 }
 
 // ---------------------------------------------------------------- f32 tile path
@@ -771,8 +969,8 @@ __global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(cons
         const int per_head = p.q_len / NC;
         ct = (y % p.G) * per_head + (per_head - 1 - y / p.G);
     }
-    int L, kv_begin, kv_end, col0, ncols, qn;
-    if (!split_prologue<NC>(p, ct, L, kv_begin, kv_end, col0, ncols, qn)) return;
+    int L, kv_begin, kv_end, col0, ncols, qn, why;
+    if (!split_prologue<NC>(p, ct, L, kv_begin, kv_end, col0, ncols, qn, why)) return;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int rg = lane / 8, kg = lane % 8;
     const int r0 = warp * 16 + rg * 4;  // this thread's first column in the tile
@@ -993,13 +1191,30 @@ cudaError_t launch_f32_instance(const SplitParams &p, cudaStream_t stream) {
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 64 && !configured[dev]) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   Lay::kBytes + Lay::kPartBytes);
         if (err != cudaSuccess) return err;
         configured[dev] = 1;
     }
     dim3 grid(p.n_chunks, p.Hkv * p.col_tiles, p.B);
-    kern<<<grid, Lay::W * 32, Lay::kBytes, stream>>>(p);
-    return cudaGetLastError();
+    if (!p.cluster) {
+        kern<<<grid, Lay::W * 32, Lay::kBytes, stream>>>(p);
+        return cudaGetLastError();
+    }
+    // one cluster per (sequence, kv head, column tile): its n_chunks (<= 8) splits
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Lay::W * 32, 1, 1);
+    cfg.dynamicSmemBytes = Lay::kBytes + Lay::kPartBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.n_chunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 int split_f32_cols_per_cta(int G, int q_len) {

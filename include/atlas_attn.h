@@ -198,9 +198,13 @@ size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_k
 
 /*
  * Keys per split-KV chunk of the call of `kind` with these arguments (the
- * chunks atlas_launch.chunk_range counts), 0 when the call has no chunks (the
- * tensor-core path writing its output directly; never with a phase other than
- * ATLAS_PHASE_ALL), -1 if the arguments are invalid.  Reads the same fields as
+ * chunks atlas_launch.chunk_range counts), 0 when the call has no chunks in
+ * the workspace (the kernel writes its output itself: the tensor-core path with
+ * many query tiles; a bf16 call with few query rows whose context per (sequence,
+ * kv head) holds at most 256 KB of K/V; an fp32 call with few query rows whose
+ * automatic plan has at most 8 splits, merged inside one thread-block cluster;
+ * never with a phase other than ATLAS_PHASE_ALL, a chunk_range or a fixed
+ * split_tokens), -1 if the arguments are invalid.  Reads the same fields as
  * atlas_attn_workspace_size.
  */
 int32_t atlas_attn_split_tokens(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,

@@ -110,7 +110,8 @@ def test_entry_points_check_arguments_before_any_launch(lib):
     L.out = fake
     args = [fake, fake, fake, fake, fake, 8, 2, 80, 16, ctypes.c_float(0.1), ctypes.byref(L)]
     assert lib.atlas_attn_decode(*args) == 2
-    # missing workspace
+    # missing workspace (a context long enough to be split: 16K keys per sequence)
+    L.max_pages_per_seq = 1024
     args = [fake, fake, fake, fake, fake, 8, 2, 128, 16, ctypes.c_float(0.1), ctypes.byref(L)]
     assert lib.atlas_attn_decode(*args) == 3
     # non-finite scale
@@ -225,3 +226,24 @@ def test_split_plan_follows_the_sm_count(lib):
     assert plan(2049, batch=2, Hq=32, Hkv=8, ctx=8192, P=64, kind=2, q_len=8192) > 0
     # a negative count is an invalid argument
     assert plan(-1) == -1
+
+
+def test_short_decode_contexts_write_their_output_directly(lib):
+    """A decode-like call whose context per (sequence, kv head) holds at most 256 KB of
+    K/V runs one split per unit that writes the output itself: no chunks, no
+    workspace.  Longer contexts, a fixed split size or a chunked phase keep the split
+    form."""
+    def both(P=16, pages=8, D=128, **kw):
+        return (ws(lib, D=D, P=P, max_pages_per_seq=pages, **kw),
+                split_tokens(lib, D=D, P=P, max_pages_per_seq=pages, **kw))
+
+    f32 = dict(q_dtype=0, kv_dtype=0, out_dtype=0)
+    # 512 keys x 2 x 64 x 4 B = 256 KB (fp32, head_dim 64, as the single-sequence decode)
+    assert both(pages=32, D=64, Hq=4, Hkv=4, **f32) == (0, 0)
+    assert both(pages=33, D=64, Hq=4, Hkv=4, **f32)[0] > 0
+    # bf16, head_dim 128: 512 keys = 256 KB
+    assert both(pages=32) == (0, 0)
+    assert both(pages=33)[0] > 0
+    # a fixed split size or a chunked phase keeps the split form
+    assert both(pages=8, split_tokens=64)[0] > 0
+    assert both(pages=8, phase=1)[1] > 0

@@ -53,8 +53,11 @@ def test_decode_bf16_parity(D, P, Hq, Hkv, lens, split):
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("split", [0, 64])
-def test_decode_f32_parity(D, split):
-    prob = small(B=4, Hq=8, Hkv=4, D=D, P=16, lens=(1, 17, 512, 777), dtype="f32", seed=D)
+@pytest.mark.parametrize("lens", [(1, 17, 512, 777), (1, 17, 300, 512)])
+def test_decode_f32_parity(D, split, lens):
+    # contexts up to 512 keys with the automatic plan: at most 8 splits, merged inside
+    # a thread-block cluster; longer ones, or split 64, go through the merge kernel
+    prob = small(B=4, Hq=8, Hkv=4, D=D, P=16, lens=lens, dtype="f32", seed=D)
     ref, ref_lse = oracle_rows(prob, want_lse=True)
     lse = torch.empty(flat_rows(prob), dtype=torch.float32, device=DEV)
     out = run_gpu(prob.to(DEV), lse=lse, split_tokens=split)
@@ -165,22 +168,28 @@ def test_deterministic_and_padding_never_read():
     assert torch.equal(a, b)
 
 
-def test_bad_page_id_flags_status_and_poisons_only_that_sequence():
-    prob = small(lens=(100, 200, 50))
+# split 0: short contexts, one split writing the output directly (bf16) or splits
+# merged inside a thread-block cluster (f32); 64: split + merge kernel
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("split", [0, 64])
+def test_bad_page_id_flags_status_and_poisons_only_that_sequence(split, dtype):
+    prob = small(lens=(100, 200, 50), dtype=dtype)
     prob.page_table[1, 3] = prob.num_pages + 7
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status)
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status, split_tokens=split)
     torch.cuda.synchronize()
     assert int(status.item()) & atlas.DEV_BAD_PAGE
     assert torch.isnan(out[1]).all()
     assert torch.isfinite(out[0]).all() and torch.isfinite(out[2]).all()
 
 
-def test_bad_seq_len_flags_status_and_poisons_rows():
-    prob = small(lens=(100, 200, 50))
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("split", [0, 64])
+def test_bad_seq_len_flags_status_and_poisons_rows(split, dtype):
+    prob = small(lens=(100, 200, 50), dtype=dtype)
     prob.seq_lens[2] = prob.max_pages * prob.page_tokens + 1
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status)
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status, split_tokens=split)
     torch.cuda.synchronize()
     assert int(status.item()) & atlas.DEV_BAD_SEQLEN
     assert torch.isnan(out[2]).all()
@@ -188,19 +197,20 @@ def test_bad_seq_len_flags_status_and_poisons_rows():
 
 
 def test_small_workspace_is_rejected():
-    prob = small().to(DEV)
+    prob = small(lens=(2000, 300, 16)).to(DEV)  # long enough to be split
     with pytest.raises(atlas.AtlasError) as e:
         run_gpu(prob, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
     assert e.value.status == 3
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("split", [0, 64])
+def test_bounded_wait_reports_timeout_and_context_survives(split):
     # The producer withholds its first stage: the consumers' bounded wait runs
     # out (about 2 s), the kernel records ATLAS_DEV_TIMEOUT and returns.
     prob = small(B=1, lens=(300,))
     dev = prob.to(DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    out = run_gpu(dev, out_dtype=torch.float32, status=status,
+    out = run_gpu(dev, out_dtype=torch.float32, status=status, split_tokens=split,
                   debug_flags=atlas.DEBUG_WITHHOLD_STAGE)
     torch.cuda.synchronize()
     assert int(status.item()) & atlas.DEV_TIMEOUT

@@ -16,7 +16,16 @@ PATHS = [
     ("decode bf16 split", lambda: inputs.make("decode", 3, 16, 4, 128, 16, [700, 45, 2100], seed=31), {}),
     ("decode bf16 split 64", lambda: inputs.make("decode", 2, 8, 2, 128, 32, [1000, 333], seed=32),
      dict(split_tokens=64)),
-    ("decode f32", lambda: inputs.make("decode", 2, 8, 4, 64, 16, [300, 77], dtype="f32", seed=33), {}),
+    # short contexts: bf16 one split writing the output directly, f32 splits merged
+    # inside a thread-block cluster; then the same f32 call split + merged
+    ("decode bf16 direct", lambda: inputs.make("decode", 3, 16, 4, 128, 16, [200, 45, 400],
+                                               seed=30), {}),
+    ("decode f32 cluster", lambda: inputs.make("decode", 2, 8, 4, 64, 16, [300, 77], dtype="f32",
+                                               seed=33), {}),
+    ("decode f32 split 64", lambda: inputs.make("decode", 2, 8, 4, 64, 16, [300, 77], dtype="f32",
+                                                seed=33), dict(split_tokens=64)),
+    ("suffix f32 cluster", lambda: inputs.make("suffix", 2, 8, 2, 128, 16, [400, 90], q_len=3,
+                                               dtype="f32", seed=29), {}),
     ("suffix split kernel", lambda: inputs.make("suffix", 2, 8, 4, 128, 16, [500, 90], q_len=4,
                                                 seed=34), {}),
     ("suffix tensor core", lambda: inputs.make("suffix", 2, 32, 4, 128, 32, [900, 300], q_len=16,
