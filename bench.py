@@ -136,10 +136,11 @@ def work_of(prob, window: int = 0):
     return kv, flops
 
 
-F32_TILE_MIN_COLS = 64  # fp32 calls with this many columns per kv head take the tile kernel
+TC_MIN_COLS = 17  # calls with more query rows per kv head take a tensor-core kernel
 KERNEL_SOURCES = {"split_bf16_kernel": "split_kv.cu", "split_f32_kernel": "split_kv.cu",
-                  "split_f32_tile_kernel": "split_kv.cu",
-                  "fmha_tc_kernel": "fmha_tc.cu"}
+                  "fmha_tc_kernel": "fmha_tc.cu", "fmha_tf32x3_kernel": "fmha_tc_f32.cu"}
+# nominal dense tf32 / bf16 tensor rates of the part (1.1 and 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
 
 
 def kernel_source_sha(kernel: str) -> str:
@@ -421,14 +422,10 @@ def measure(args, index, world, rank, local, e2e=True, cpu_budget=12.0):
         achieved = flops / (main_avg * 1e-3) / 1e12
         peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
         bound = "tensor"
-    tc_path = prob.dtype == "bf16" and \
-        prob.q_len * (prob.n_q_heads // prob.n_kv_heads) > 16
-    f32_tile = prob.dtype == "f32" and \
-        prob.q_len * (prob.n_q_heads // prob.n_kv_heads) >= F32_TILE_MIN_COLS
+    tc_path = prob.q_len * (prob.n_q_heads // prob.n_kv_heads) >= TC_MIN_COLS
+    f32_tc = tc_path and prob.dtype == "f32"
     if tc_path:
-        kernel = "fmha_tc_kernel"
-    elif f32_tile:
-        kernel = "split_f32_tile_kernel"
+        kernel = "fmha_tc_kernel" if prob.dtype == "bf16" else "fmha_tf32x3_kernel"
     else:
         kernel = "split_bf16_kernel" if prob.dtype == "bf16" else "split_f32_kernel"
     # launches per step: the main kernel, plus the merge unless the tensor-core
@@ -437,16 +434,16 @@ def measure(args, index, world, rank, local, e2e=True, cpu_budget=12.0):
     # no workspace: the main kernel wrote the output itself (tensor-core direct mode,
     # a short bf16 context in one split, fp32 splits merged inside a cluster)
     launches_per_step = 1 if ws_bytes == 0 else 2
-    if f32_tile:
-        # many-row fp32 work runs on the FFMA pipe: SMs x 128 FMA / clock x 2 flops
-        # at the SM clock sampled under load (nominal max 2070 MHz if none)
-        clk_now = clocks.summary(t_begin, t_end + 0.05) or \
-            clocks.summary(t_begin - 0.5, t_end + 0.05)
-        mhz = clk_now["sm_mhz"] if clk_now else 2070.0
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+    if f32_tc:
+        # fp32 on the tensor cores as three tf32 products per fp32 product: the
+        # ceiling is a third of the tf32 peak (the measured bf16 peak x 1.1 / 2.25);
+        # achieved counts algorithmic flops
+        tf32 = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * TF32_PER_BF16
+        peak = tf32 / 3
         achieved = flops / (main_avg * 1e-3) / 1e12
-        bound, pk_kind = "alu", f"FFMA pipe: {sms} SMs x 128 FMA/clk x 2 x {mhz:.0f} MHz"
+        bound = "tensor"
+        pk_kind = (f"{pk_kind} bf16 x 1.1/2.25 = {tf32:.1f} TFLOP/s tf32, / 3 tf32 products "
+                   "per fp32 product")
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -488,7 +485,7 @@ def measure(args, index, world, rank, local, e2e=True, cpu_budget=12.0):
             "achieved": round(achieved, 3),
             "peak": peak,
             "peak_source": pk_kind,
-            "unit": "TFLOP/s" if f32_tile else unit,
+            "unit": "TFLOP/s" if f32_tc else unit,
             "frac": round(achieved / peak, 4),
             "traffic": workload_traffic(args, kernel, cfg["name"]),
         },

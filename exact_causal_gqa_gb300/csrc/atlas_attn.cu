@@ -62,12 +62,6 @@ int64_t tc_direct_tiles(int sms) { return (int64_t)sms * 2; }
 constexpr int kHiLoBelow = 512;
 constexpr float kHiLoScale = 1.25f;
 
-// fp32 calls with at least this many columns (G x q_len) per (sequence, kv head)
-// take the 128-column tile kernel; its splits aim for about 8 waves of one CTA
-// per SM (its CTAs are long: 32-key blocks of 128 x D x 2 FFMA each).
-constexpr int kF32TileMinCols = 64;
-int64_t f32_tile_plan_ctas(int sms) { return (int64_t)sms * 8; }
-
 // A bf16 decode-like call whose whole context per (sequence, kv head) holds at most
 // this many K/V bytes runs as one split per (sequence, kv head, column tile) that
 // writes its output directly: at that size the merge launch (a few microseconds)
@@ -145,9 +139,10 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
     plan->direct = plan->cluster = 0;
     plan->tc_split = 0;
     plan->tiles_per_unit = plan->tiles_per_head = 0;
-    if (L->kv_dtype == ATLAS_BF16 && (int64_t)G * L->q_len > 16) {
-        // Many query rows per (sequence, kv head): 128-row tiles on tcgen05.
-        plan->path = Path::TensorCore;
+    if ((int64_t)G * L->q_len > 16) {
+        // Many query rows per (sequence, kv head): 128-row tiles on tcgen05 (bf16
+        // products, or three tf32 products per fp32 product).
+        plan->path = L->kv_dtype == ATLAS_BF16 ? Path::TensorCore : Path::TensorCoreF32;
         const int64_t tiles_per_unit = ((int64_t)G * L->q_len + 127) / 128;
         const int64_t tiles = (int64_t)L->batch * Hkv * tiles_per_unit;
         if ((int64_t)L->batch * Hq * L->q_len >= INT32_MAX) return ATLAS_ERR_INVALID_ARG;
@@ -182,10 +177,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         return ATLAS_OK;
     }
     plan->path = L->kv_dtype == ATLAS_BF16 ? Path::SplitBF16 : Path::SplitF32;
-    if (plan->path == Path::SplitF32 && (int64_t)G * L->q_len >= kF32TileMinCols)
-        plan->path = Path::SplitF32Tile;
     const int cols = plan->path == Path::SplitBF16      ? split_bf16_cols_per_cta(G, L->q_len)
-                     : plan->path == Path::SplitF32Tile ? split_f32_tile_cols()
                                                         : split_f32_cols_per_cta(G, L->q_len);
     plan->col_tiles = (G * L->q_len + cols - 1) / cols;
     if ((int64_t)Hkv * plan->col_tiles > 65535 || L->batch > 65535) return ATLAS_ERR_UNSUPPORTED;
@@ -200,13 +192,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         plan->acc_bytes = plan->ml_offset = plan->ws_bytes = 0;
         return ATLAS_OK;
     }
-    if (chunk == 0 && plan->path == Path::SplitF32Tile) {
-        const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
-        const int64_t target = f32_tile_plan_ctas(sms);
-        chunk = round_up((work_ctx * units + target - 1) / target, kSplitBlockTokens);
-        if (chunk < 512) chunk = 512;
-        if (chunk > 16384) chunk = 16384;
-    } else if (chunk == 0) {
+    if (chunk == 0) {
         const int64_t units = (int64_t)L->batch * Hkv * plan->col_tiles;
         const int64_t target =
             plan->path == Path::SplitF32 && cols <= 8 ? f32_ring_plan_ctas(sms) : plan_ctas(sms);
@@ -234,20 +220,21 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
 
 namespace {
 
-// 2-D view of a bf16 tensor with D elements per row: `rows` rows; boxes of 64
-// elements x box_rows rows with 128-byte swizzling.
+// 2-D view of a bf16 (or fp32) tensor with D elements per row: `rows` rows; boxes
+// of one 128-byte row slab (64 bf16 or 32 fp32 elements) x box_rows rows with
+// 128-byte swizzling.
 atlas_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int32_t D,
-                             int32_t box_rows) {
+                             int32_t box_rows, bool f32 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return ATLAS_ERR_CUDA;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * (f32 ? 4 : 2)};
+    const cuuint32_t box[2] = {f32 ? 32u : 64u, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 
@@ -349,14 +336,16 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     if (L->phase == ATLAS_PHASE_MERGE) {
         if (ev[0] && cudaEventRecord(ev[0], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
         if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
-    } else if (plan.path == Path::TensorCore) {
+    } else if (plan.path == Path::TensorCore || plan.path == Path::TensorCoreF32) {
         CUtensorMap tmQ, tmK, tmV;
-        const int box = P < 128 ? P : 128;
-        st = encode_rows_map(&tmQ, q, (int64_t)L->batch * Hq * L->q_len, D, 128);
+        const bool f32 = plan.path == Path::TensorCoreF32;
+        const int bn = f32 ? 64 : 128;  // keys per block of the kernel
+        const int box = P < bn ? P : bn;
+        st = encode_rows_map(&tmQ, q, (int64_t)L->batch * Hq * L->q_len, D, 128, f32);
         if (st == ATLAS_OK)
-            st = encode_rows_map(&tmK, k_pages, (int64_t)L->num_pages * Hkv * P, D, box);
+            st = encode_rows_map(&tmK, k_pages, (int64_t)L->num_pages * Hkv * P, D, box, f32);
         if (st == ATLAS_OK)
-            st = encode_rows_map(&tmV, v_pages, (int64_t)L->num_pages * Hkv * P, D, box);
+            st = encode_rows_map(&tmV, v_pages, (int64_t)L->num_pages * Hkv * P, D, box, f32);
         if (st != ATLAS_OK) return st;
         TcParams tp{};
         tp.page_table = page_table;
@@ -392,7 +381,8 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         tp.ws_ml = sp.ws_ml;
         tp.status = L->status_word;
         if (ev[0] && cudaEventRecord(ev[0], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
-        err = launch_fmha_tc(tp, tmQ, tmK, tmV, stream);
+        err = f32 ? launch_fmha_tc_f32(tp, tmQ, tmK, tmV, stream)
+                  : launch_fmha_tc(tp, tmQ, tmK, tmV, stream);
         if (err != cudaSuccess) return ATLAS_ERR_CUDA;
         if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
         if (!plan.tc_split) {
@@ -407,8 +397,6 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         if (st == ATLAS_OK) st = encode_pool_map(&tmV, v_pages, L->num_pages, Hkv, P, D);
         if (st != ATLAS_OK) return st;
         err = launch_split_bf16(sp, tmK, tmV, stream);
-    } else if (plan.path == Path::SplitF32Tile) {
-        err = launch_split_f32_tile(sp, stream);
     } else {
         err = launch_split_f32(sp, stream);
     }

@@ -69,7 +69,8 @@ struct MergeParams {
 };
 
 // Tensor-core (tcgen05 / TMEM) path for many query rows per (sequence, kv head):
-// 128-row query tiles x 128-key blocks, head_dim 64 or 128, bf16.  Either writes the
+// 128-row query tiles x 128-key blocks (bf16) or 64-key blocks (fp32 as 3 x tf32),
+// head_dim 64 or 128.  Either writes the
 // normalised output directly (one CTA per tile, all its keys) or, when there are
 // too few tiles to fill the GPU, split partials in the SplitParams layout.
 struct TcParams {
@@ -109,6 +110,9 @@ cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t stream);
 
 cudaError_t launch_fmha_tc(const TcParams &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                            const CUtensorMap &tmV, cudaStream_t stream);
+// The same for fp32 q/K/V: three tf32 products per fp32 product (fmha_tc_f32.cu).
+cudaError_t launch_fmha_tc_f32(const TcParams &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                               const CUtensorMap &tmV, cudaStream_t stream);
 
 // Columns handled by one CTA of the bf16 split kernel.
 int split_bf16_cols_per_cta(int G, int q_len);
@@ -118,9 +122,6 @@ cudaError_t launch_split_bf16(const SplitParams &p, const CUtensorMap &tmK, cons
 // fp32 with few columns: 4, 8 or 16 columns per CTA by G x q_len.
 int split_f32_cols_per_cta(int G, int q_len);
 cudaError_t launch_split_f32(const SplitParams &p, cudaStream_t stream);
-// fp32 with many columns per (sequence, kv head): 128-column register-tiled FFMA.
-int split_f32_tile_cols();
-cudaError_t launch_split_f32_tile(const SplitParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 
 // Multiprocessor count of the current device (cached per device); 152 (one
@@ -130,7 +131,7 @@ int device_sm_count();
 // The split plan of a call: which kernel path, split geometry and workspace.  A
 // pure function of the call's sizes and the SM count (atlas_launch.sm_count, else
 // device_sm_count()).
-enum class Path { SplitBF16, SplitF32, SplitF32Tile, TensorCore };
+enum class Path { SplitBF16, SplitF32, TensorCore, TensorCoreF32 };
 
 struct Plan {
     Path path;

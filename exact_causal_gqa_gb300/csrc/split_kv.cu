@@ -918,236 +918,6 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
     write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, qn, false);
 }
 
-// ---------------------------------------------------------------- f32 tile path
-// Many query rows per (sequence, kv head) in fp32 (suffix, prefill): 128 columns
-// per CTA against 64-key blocks, both contractions as register-tiled FFMA.
-// Warp w owns columns 16w .. 16w+15; lane (rg = lane / 8, kg = lane % 8) holds
-//   S for columns 16w + 4rg .. +3 and keys kg + 8c (c < 8) of the block,
-//   O for the same columns and dims 4kg + 32i .. +3 (i < D/32),
-// so a column's running max, sum and rescale stay within its 8 lanes.  K blocks
-// arrive by cp.async double-buffered; the single V buffer is refilled right after
-// the PV product and waited for just before the next one, so its load overlaps the
-// next scores.  Keys past the split's end are zero-filled (never read).  P goes
-// through shared memory transposed (P^T[key][column]) to the lanes that own the
-// same columns' O.  Strides are padded by 4 floats so that the 16-byte reads of K,
-// V and P^T are free of bank conflicts; Q reads are quarter-warp broadcasts.  The
-// kernel is bound by shared-memory wavefronts: the 4 x 8 S tile reads 12 of them
-// per 128 FMAs.
-constexpr int kF32TileCols = 128;
-constexpr int kF32TileKeys = 64;
-constexpr int kF32TileThreads = 256;
-
-template <int D>
-struct F32TileLayout {
-    static constexpr int QS = D + 4;                  // Q row stride (floats)
-    static constexpr int KS = D + 4;                  // K / V row stride
-    static constexpr int PS = kF32TileCols + 4;       // P^T row stride
-    static constexpr int kQ = kF32TileCols * QS;
-    static constexpr int kKV = kF32TileKeys * KS;     // one K or V block
-    static constexpr int kP = kF32TileKeys * PS;
-    static constexpr int kBytes = (kQ + 3 * kKV + kP) * 4;  // Q, K[2], V, P^T
-    static_assert(kBytes <= 232448, "shared memory budget");
-};
-
-template <int D>
-__global__ void __launch_bounds__(kF32TileThreads, 1) split_f32_tile_kernel(const SplitParams p) {
-    using Lay = F32TileLayout<D>;
-    constexpr int NC = kF32TileCols, BK = kF32TileKeys;
-    constexpr int OD = D / 32;  // float4 groups of O per thread
-    constexpr int DV4 = D / 4;  // float4s per K / V / Q row
-    extern __shared__ __align__(16) float f32_smem[];
-    float *sQ = f32_smem;
-    float *sK = sQ + Lay::kQ;
-    float *sV = sK + 2 * Lay::kKV;
-    float *sP = sV + Lay::kKV;
-
-    // Prefill-shaped calls (q_len a multiple of the tile): late prompt rows, which
-    // see the most keys, first.
-    const int y = blockIdx.y % p.col_tiles;
-    int ct = y;
-    if (p.q_len % NC == 0 && p.G * p.q_len == p.col_tiles * NC) {
-        const int per_head = p.q_len / NC;
-        ct = (y % p.G) * per_head + (per_head - 1 - y / p.G);
-    }
-    int L, kv_begin, kv_end, col0, ncols, qn, why;
-    if (!split_prologue<NC>(p, ct, L, kv_begin, kv_end, col0, ncols, qn, why)) return;
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int rg = lane / 8, kg = lane % 8;
-    const int r0 = warp * 16 + rg * 4;  // this thread's first column in the tile
-    const int b = blockIdx.z;
-    const int hkv = blockIdx.y / p.col_tiles;
-    const float *kp = static_cast<const float *>(p.k_pages);
-    const float *vp = static_cast<const float *>(p.v_pages);
-    const int32_t *ptab = p.page_table + (int64_t)b * p.max_pages;
-
-    // Q tile (columns past ncols and padding rows of a ragged batch: zeros).
-    for (int idx = tid; idx < NC * DV4; idx += kF32TileThreads) {
-        const int c = idx / DV4, d4 = idx % DV4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < ncols && (col0 + c) % p.q_len < qn)
-            v = reinterpret_cast<const float4 *>(static_cast<const float *>(p.q) +
-                                                 column_row(p, b, hkv, col0 + c) * D)[d4];
-        *reinterpret_cast<float4 *>(sQ + c * Lay::QS + 4 * d4) = v;
-    }
-    int lim[4], lo[4];
-    bool valid[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int c = r0 + r;
-        valid[r] = c < ncols && (col0 + c) % p.q_len < qn;
-        lim[r] = valid[r] ? min(kv_end, column_visible(p, L, col0 + c)) : kv_begin;
-        lo[r] = valid[r] ? column_first(p, L, col0 + c) : 0;
-    }
-
-    // Keys kb .. kb+BK-1 of K (into buffer buf) or V (the single V buffer).
-    auto load_rows = [&](const float *src, float *dst, int kb) {
-        const uint32_t d0 = smem_u32(dst);
-        for (int idx = tid; idx < BK * DV4; idx += kF32TileThreads) {
-            const int kr = idx / DV4, d4 = idx % DV4;
-            const int t = kb + kr;
-            const bool in = t < kv_end;
-            const int tt = in ? t : kv_begin;
-            const int64_t row = ((int64_t)ptab[tt / p.P] * p.Hkv + hkv) * p.P + tt % p.P;
-            cp_async16(d0 + (uint32_t)(kr * Lay::KS + 4 * d4) * 4u, src + row * D + 4 * d4,
-                       in ? 16u : 0u);
-        }
-    };
-
-    float4 o[4][OD];
-    float m_run[4], l_part[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        m_run[r] = -INFINITY;
-        l_part[r] = 0.f;
-#pragma unroll
-        for (int i = 0; i < OD; ++i) o[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-
-    const int nb = (kv_end - kv_begin + BK - 1) / BK;
-    // cp.async groups, in commit order: K0, V0, then per block K(j+1) after the
-    // scores start and V(j+1) after the PV product; "all but the newest group
-    // complete" is then K(j) at the top of block j and V(j) before its PV product.
-    load_rows(kp, sK, kv_begin);
-    cp_async_commit();
-    load_rows(vp, sV, kv_begin);
-    cp_async_commit();
-    for (int j = 0; j < nb; ++j) {
-        const int kb = kv_begin + j * BK;
-        cp_async_wait<1>();
-        __syncthreads();
-        if (j + 1 < nb) load_rows(kp, sK + ((j + 1) & 1) * Lay::kKV, kb + BK);
-        cp_async_commit();
-        const float *cK = sK + (j & 1) * Lay::kKV;
-
-        // S = Q K^T for 4 columns x 8 keys
-        float s[4][8];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) s[r][c] = 0.f;
-#pragma unroll 2
-        for (int d = 0; d < D; d += 4) {
-            float4 q4[4], k4[8];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                q4[r] = *reinterpret_cast<const float4 *>(sQ + (r0 + r) * Lay::QS + d);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                k4[c] = *reinterpret_cast<const float4 *>(cK + (kg + 8 * c) * Lay::KS + d);
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    s[r][c] = fmaf(q4[r].x, k4[c].x, s[r][c]);
-                    s[r][c] = fmaf(q4[r].y, k4[c].y, s[r][c]);
-                    s[r][c] = fmaf(q4[r].z, k4[c].z, s[r][c]);
-                    s[r][c] = fmaf(q4[r].w, k4[c].w, s[r][c]);
-                }
-        }
-        // scores in log2 units, masked; block max per column over the 8 lanes
-        float corr[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int t = kb + kg + 8 * c;
-                s[r][c] = (t < lim[r] && t >= lo[r]) ? score_log2(p, s[r][c]) : -INFINITY;
-                mx = fmaxf(mx, s[r][c]);
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            const float m_new = fmaxf(m_run[r], mx);
-            const float mref = m_new == -INFINITY ? 0.f : m_new;
-            corr[r] = ex2(m_run[r] - mref);  // 0 while nothing was visible
-            m_run[r] = m_new;
-            float sum = 0.f;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                s[r][c] = ex2(s[r][c] - mref);
-                sum += s[r][c];
-            }
-            l_part[r] = fmaf(l_part[r], corr[r], sum);
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<float4 *>(sP + (kg + 8 * c) * Lay::PS + r0) =
-                make_float4(s[0][c], s[1][c], s[2][c], s[3][c]);
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int i = 0; i < OD; ++i) {
-                o[r][i].x *= corr[r];
-                o[r][i].y *= corr[r];
-                o[r][i].z *= corr[r];
-                o[r][i].w *= corr[r];
-            }
-        cp_async_wait<1>();  // V(j): every group but K(j+1)
-        __syncthreads();     // V(j) from every thread; P^T of this warp's columns
-        // O += P V
-#pragma unroll 4
-        for (int t = 0; t < BK; ++t) {
-            const float4 p4 = *reinterpret_cast<const float4 *>(sP + t * Lay::PS + r0);
-            const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-            for (int i = 0; i < OD; ++i) {
-                const float4 v4 =
-                    *reinterpret_cast<const float4 *>(sV + t * Lay::KS + 4 * kg + 32 * i);
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    o[r][i].x = fmaf(pr[r], v4.x, o[r][i].x);
-                    o[r][i].y = fmaf(pr[r], v4.y, o[r][i].y);
-                    o[r][i].z = fmaf(pr[r], v4.z, o[r][i].z);
-                    o[r][i].w = fmaf(pr[r], v4.w, o[r][i].w);
-                }
-            }
-        }
-        __syncthreads();  // every warp is done with V (and this K buffer) before refills
-        if (j + 1 < nb) load_rows(vp, sV, kb + BK);
-        cp_async_commit();
-    }
-    cp_async_wait<0>();
-
-    // partial state per column: (m, l, acc) of this split
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        float l = l_part[r];
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        l += __shfl_xor_sync(0xffffffffu, l, 4);
-        if (!valid[r]) continue;
-        const int64_t slot = column_row(p, b, hkv, col0 + r0 + r) * p.n_chunks + blockIdx.x;
-        float *acc = p.ws_acc + slot * D;
-#pragma unroll
-        for (int i = 0; i < OD; ++i) *reinterpret_cast<float4 *>(acc + 4 * kg + 32 * i) = o[r][i];
-        if (kg == 0) {
-            p.ws_ml[slot * 2] = m_run[r];
-            p.ws_ml[slot * 2 + 1] = l;
-        }
-    }
-}
-
 template <int D, int NT, int STAGES>
 cudaError_t launch_bf16_instance(const SplitParams &p, const CUtensorMap &tmK,
                                  const CUtensorMap &tmV, cudaStream_t stream) {
@@ -1232,31 +1002,6 @@ cudaError_t launch_split_f32(const SplitParams &p, cudaStream_t stream) {
     return nc == 4   ? launch_f32_instance<64, 4>(p, stream)
            : nc == 8 ? launch_f32_instance<64, 8>(p, stream)
                      : launch_f32_instance<64, 16>(p, stream);
-}
-
-template <int D>
-cudaError_t launch_f32_tile_instance(const SplitParams &p, cudaStream_t stream) {
-    auto kern = split_f32_tile_kernel<D>;
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    if (dev < 64 && !configured[dev]) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   F32TileLayout<D>::kBytes);
-        if (err != cudaSuccess) return err;
-        configured[dev] = 1;
-    }
-    dim3 grid(p.n_chunks, p.Hkv * p.col_tiles, p.B);
-    kern<<<grid, kF32TileThreads, F32TileLayout<D>::kBytes, stream>>>(p);
-    return cudaGetLastError();
-}
-
-int split_f32_tile_cols() { return kF32TileCols; }
-
-cudaError_t launch_split_f32_tile(const SplitParams &p, cudaStream_t stream) {
-    return p.D == 128 ? launch_f32_tile_instance<128>(p, stream)
-                      : launch_f32_tile_instance<64>(p, stream);
 }
 
 }  // namespace atlas

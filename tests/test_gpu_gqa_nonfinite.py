@@ -54,7 +54,7 @@ def test_gqa_equals_mha_with_duplicated_heads(kind, dtype, Hq, Hkv, D, P, q_len,
 @pytest.mark.parametrize("kind,dtype,Hq,Hkv,D,P,q_len", [
     ("suffix", "bf16", 32, 4, 128, 32, 16),   # tensor cores (G * q_len = 128)
     ("suffix", "bf16", 8, 4, 128, 16, 4),     # split kernel (G * q_len = 8)
-    ("suffix", "f32", 16, 2, 128, 16, 16),    # fp32 tile kernel
+    ("suffix", "f32", 16, 2, 128, 16, 16),    # fp32 tensor-core kernel (3 x tf32)
     ("suffix", "f32", 4, 2, 64, 16, 2),       # fp32 ring kernel
 ])
 def test_nan_key_reaches_exactly_the_rows_that_see_it(kind, dtype, Hq, Hkv, D, P, q_len):

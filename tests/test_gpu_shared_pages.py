@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
     ("suffix", "bf16", 32, 4, 128, 32, 16, (3000, 2600, 3000), 50),   # tcgen05, split + merge
     ("prefill", "bf16", 8, 2, 128, 64, 300, (300, 300, 300), 3),       # tcgen05, direct
     ("decode", "f32", 8, 4, 64, 16, 1, (900, 700, 900), 20),           # fp32 ring kernel
-    ("suffix", "f32", 16, 2, 128, 16, 16, (1200, 1000, 1200), 30),     # fp32 tile kernel
+    ("suffix", "f32", 16, 2, 128, 16, 16, (1200, 1000, 1200), 30),     # fp32 tensor-core kernel (3 x tf32)
 ])
 def test_shared_prefix_pages(kind, dtype, Hq, Hkv, D, P, q_len, lens, shared):
     host = inputs.make(kind, 3, Hq, Hkv, D, P, list(lens), q_len=q_len, dtype=dtype,
