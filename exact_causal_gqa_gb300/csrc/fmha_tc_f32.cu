@@ -444,93 +444,106 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
         float *m_run_s = reinterpret_cast<float *>(smem + C::OFF_MRUN);
         float m_run = -INFINITY;
         bool ok = wait_warp(BAR(C::B_QREADY), 0, abort_flag);  // Q staging consumed
-        for (int j = 0; ok && j < nb; ++j) {
+        // K lo of block j, same layout as the raw block, and K's hi part in place:
+        // element-wise on 16-byte chunks (no S product of the block is issued yet).
+        auto convert_k = [&](int j) -> bool {
             const int s = j % S, use = j / S;
-            // K lo, same layout as the raw block, and K's hi part in place: element-wise
-            // on 16-byte chunks (no S product of this block has been issued yet).
             if (!wait_warp(BAR(C::B_KFULL + s), use & 1, abort_flag) ||
-                (j > 0 && !wait_warp(BAR(C::B_KLO_FREE), (j - 1) & 1, abort_flag))) {
-                ok = false;
-                break;
-            }
-            {
-                float4 *src = reinterpret_cast<float4 *>(smem + C::OFF_K + s * C::kBlkBytes);
-                float4 *dst = reinterpret_cast<float4 *>(smem + C::OFF_KLO);
-                for (int k = ct; k < C::kBlkBytes / 16; k += 128) {
-                    const float4 x = src[k];
-                    dst[k] = make_float4(tf32_lo(x.x), tf32_lo(x.y), tf32_lo(x.z), tf32_lo(x.w));
-                    src[k] = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
-                }
+                (j > 0 && !wait_warp(BAR(C::B_KLO_FREE), (j - 1) & 1, abort_flag)))
+                return false;
+            float4 *src = reinterpret_cast<float4 *>(smem + C::OFF_K + s * C::kBlkBytes);
+            float4 *dst = reinterpret_cast<float4 *>(smem + C::OFF_KLO);
+            for (int k = ct; k < C::kBlkBytes / 16; k += 128) {
+                const float4 x = src[k];
+                dst[k] = make_float4(tf32_lo(x.x), tf32_lo(x.y), tf32_lo(x.z), tf32_lo(x.w));
+                src[k] = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
             }
             fence_proxy_async_smem();
             mbar_arrive(BAR(C::B_KLO_READY));
-            // V^T hi / lo: 4 keys x 4 dims per step, transposed in registers.
+            return true;
+        };
+        // V^T hi / lo of block j: 4 keys x 4 dims per lane and step, transposed in
+        // registers.  Warp step it covers key groups kq0 .. kq0+7 x dim groups
+        // dq0 .. dq0+3 (lane: kq = kq0 + lane % 8, dq = dq0 + lane / 8): the 16-byte
+        // reads of a step fall on 8 distinct chunks of 4 rows, the writes on 8 chunks
+        // of 4 rows of V^T, so neither conflicts beyond its 4 wavefronts.
+        auto convert_v = [&](int j) -> bool {
+            const int s = j % S, use = j / S;
             if (!wait_warp(BAR(C::B_VFULL + s), use & 1, abort_flag) ||
-                (j > 0 && !wait_warp(BAR(C::B_VT_FREE), (j - 1) & 1, abort_flag))) {
-                ok = false;
-                break;
-            }
-            {
-                // Warp step it covers key groups kq0 .. kq0+7 x dim groups dq0 .. dq0+3
-                // (lane: kq = kq0 + lane % 8, dq = dq0 + lane / 8): the 16-byte reads of
-                // a step fall on 8 distinct chunks of 4 rows, the writes on 8 chunks of 4
-                // rows of V^T, so neither conflicts beyond its 4 wavefronts.
-                const int valid = min(BN, kv_end - (kv_begin + j * BN));  // keys in this block
-                const uint8_t *vraw = smem + C::OFF_V + s * C::kBlkBytes;
-                constexpr int kSteps = (BN / 32) * (D / 16);  // warp steps per block
-                for (int it = warp - C::kConvWarp0; it < kSteps; it += 4) {
-                    const int kq = (it % (BN / 32)) * 8 + lane % 8;   // 4-key group
-                    const int dq = (it / (BN / 32)) * 4 + lane / 8;   // 4-dim group
-                    float v[4][4];  // [key][dim]
+                (j > 0 && !wait_warp(BAR(C::B_VT_FREE), (j - 1) & 1, abort_flag)))
+                return false;
+            const int valid = min(BN, kv_end - (kv_begin + j * BN));  // keys in this block
+            const uint8_t *vraw = smem + C::OFF_V + s * C::kBlkBytes;
+            constexpr int kSteps = (BN / 32) * (D / 16);  // warp steps per block
+            for (int it = warp - C::kConvWarp0; it < kSteps; it += 4) {
+                const int kq = (it % (BN / 32)) * 8 + lane % 8;  // 4-key group
+                const int dq = (it / (BN / 32)) * 4 + lane / 8;  // 4-dim group
+                float v[4][4];                                    // [key][dim]
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int key = 4 * kq + e;
-                        const int d0 = 4 * dq;
-                        // raw: slab d0/32, row key, 16-byte chunk (d0 % 32) / 4
-                        const uint32_t off = (d0 / 32) * C::kKSlab + sw128(key, (d0 % 32) / 4);
-                        const float4 x = *reinterpret_cast<const float4 *>(vraw + off);
-                        const bool in = key < valid;
-                        v[e][0] = in ? x.x : 0.f;
-                        v[e][1] = in ? x.y : 0.f;
-                        v[e][2] = in ? x.z : 0.f;
-                        v[e][3] = in ? x.w : 0.f;
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    const int key = 4 * kq + e;
+                    const int d0 = 4 * dq;
+                    // raw: slab d0/32, row key, 16-byte chunk (d0 % 32) / 4
+                    const uint32_t off = (d0 / 32) * C::kKSlab + sw128(key, (d0 % 32) / 4);
+                    const float4 x = *reinterpret_cast<const float4 *>(vraw + off);
+                    const bool in = key < valid;
+                    v[e][0] = in ? x.x : 0.f;
+                    v[e][1] = in ? x.y : 0.f;
+                    v[e][2] = in ? x.z : 0.f;
+                    v[e][3] = in ? x.w : 0.f;
+                }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int dim = 4 * dq + e;
-                        const int k0 = 4 * kq;
-                        // V^T: slab k0/32, row dim, 16-byte chunk (k0 % 32) / 4
-                        const uint32_t off = (k0 / 32) * C::kVtSlab + sw128(dim, (k0 % 32) / 4);
-                        *reinterpret_cast<float4 *>(smem + C::OFF_VTH + off) =
-                            make_float4(tf32_hi(v[0][e]), tf32_hi(v[1][e]), tf32_hi(v[2][e]),
-                                        tf32_hi(v[3][e]));
-                        *reinterpret_cast<float4 *>(smem + C::OFF_VTL + off) =
-                            make_float4(tf32_lo(v[0][e]), tf32_lo(v[1][e]), tf32_lo(v[2][e]),
-                                        tf32_lo(v[3][e]));
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    const int dim = 4 * dq + e;
+                    const int k0 = 4 * kq;
+                    // V^T: slab k0/32, row dim, 16-byte chunk (k0 % 32) / 4
+                    const uint32_t off = (k0 / 32) * C::kVtSlab + sw128(dim, (k0 % 32) / 4);
+                    *reinterpret_cast<float4 *>(smem + C::OFF_VTH + off) =
+                        make_float4(tf32_hi(v[0][e]), tf32_hi(v[1][e]), tf32_hi(v[2][e]),
+                                    tf32_hi(v[3][e]));
+                    *reinterpret_cast<float4 *>(smem + C::OFF_VTL + off) =
+                        make_float4(tf32_lo(v[0][e]), tf32_lo(v[1][e]), tf32_lo(v[2][e]),
+                                    tf32_lo(v[3][e]));
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(BAR(C::B_VT_READY));
             mbar_arrive(BAR(C::B_VEMPTY + s));
-            if (j % kSegBlocks == 0 && j > 0) {
-                // Fold segment g (blocks before j) into the running sum: read it out of
-                // TMEM (the next PV overwrites it once every thread here has), then
-                // O_run = O_run 2^(m_run - m_seg) + O_seg in fp32.
-                const int g = j / kSegBlocks - 1;
+            return true;
+        };
+        // Order: V^T of block j; at a segment's first block the previous segment is
+        // read out of TMEM (the next PV overwrites it once every thread here has); K lo
+        // of block j + 1 (S(j + 1) waits for it); then the fold of that segment,
+        // O_run = O_run 2^(m_run - m_seg) + O_seg in fp32, off the S path.
+        ok = ok && convert_k(0);
+        for (int j = 0; ok && j < nb; ++j) {
+            if (!convert_v(j)) {
+                ok = false;
+                break;
+            }
+            const bool fold = j % kSegBlocks == 0 && j > 0;
+            const int g = j / kSegBlocks - 1;  // the segment folded at block j
+            uint32_t o[D / 32][32];
+            float m_seg = -INFINITY;
+            if (fold) {
                 if (!wait_warp(BAR(C::B_SEG_DONE), g & 1, abort_flag) ||
                     !wait_warp(BAR(C::B_MSEG), g & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t o[D / 32][32];
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tq + 32 * cc, o[cc]);
                 tmem_wait_ld();
-                const float m_seg = m_seg_s[(g & 1) * BM + r];
+                m_seg = m_seg_s[(g & 1) * BM + r];
                 tc_fence_before();
                 mbar_arrive(BAR(C::B_O_DRAINED));
+            }
+            if (j + 1 < nb && !convert_k(j + 1)) {
+                ok = false;
+                break;
+            }
+            if (fold) {
                 if (row_ok) {
                     const float fr = g == 0 || m_run == -INFINITY ? 0.f : ex2(m_run - m_seg);
 #pragma unroll
@@ -623,12 +636,21 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
                 sr[e] = __uint_as_float(sa[e]);
                 sr[32 + e] = __uint_as_float(sb2[e]);
             }
+            // Blocks whose every column is visible to every real row of the warp skip
+            // the masks (padding rows never reach the output).
+            const bool all_visible = __all_sync(0xffffffffu, !valid || (nvis >= BN && nlo <= 0));
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (all_visible) {
 #pragma unroll
-            for (int e = 0; e < BN; e += 2) {
-                const float v0 = e < nvis && e >= nlo ? sr[e] : -INFINITY;
-                const float v1 = e + 1 < nvis && e + 1 >= nlo ? sr[e + 1] : -INFINITY;
-                m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], v0, v1);
+                for (int e = 0; e < BN; e += 2)
+                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], sr[e], sr[e + 1]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < BN; e += 2) {
+                    const float v0 = e < nvis && e >= nlo ? sr[e] : -INFINITY;
+                    const float v1 = e + 1 < nvis && e + 1 >= nlo ? sr[e + 1] : -INFINITY;
+                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], v0, v1);
+                }
             }
             const float mraw = valid ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) : -INFINITY;
             const float mx = mraw == -INFINITY ? -INFINITY
@@ -647,32 +669,40 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
             for (int k = 0; k < 4; ++k) rs2[k] = make_float2(0.f, 0.f);
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-mref, -mref);
+            auto make_p = [&](bool masked, bool cap) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t ph[32], pl[32];
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t ph[32], pl[32];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int c0 = 32 * half + 2 * k;
-                    const float a0 = sr[c0], a1 = sr[c0 + 1];
-                    float2 t;
-                    if (capped) {
-                        t.x = p.softcap_log2 * tanh_acc(a0 * p.softcap_inv) - mref;
-                        t.y = p.softcap_log2 * tanh_acc(a1 * p.softcap_inv) - mref;
-                    } else {
-                        t = ffma2(make_float2(a0, a1), sc2, nm2);
+                    for (int k = 0; k < 16; ++k) {
+                        const int c0 = 32 * half + 2 * k;
+                        const float a0 = sr[c0], a1 = sr[c0 + 1];
+                        float2 t;
+                        if (cap) {
+                            t.x = p.softcap_log2 * tanh_acc(a0 * p.softcap_inv) - mref;
+                            t.y = p.softcap_log2 * tanh_acc(a1 * p.softcap_inv) - mref;
+                        } else {
+                            t = ffma2(make_float2(a0, a1), sc2, nm2);
+                        }
+                        if (masked) {
+                            t.x = c0 < nvis && c0 >= nlo ? t.x : -INFINITY;
+                            t.y = c0 + 1 < nvis && c0 + 1 >= nlo ? t.y : -INFINITY;
+                        }
+                        const float2 e2 = make_float2(ex2(t.x), ex2(t.y));
+                        rs2[k & 3] = fadd2(rs2[k & 3], e2);
+                        const float2 hi = make_float2(tf32_hi(e2.x), tf32_hi(e2.y));
+                        const float2 lo = fadd2(e2, make_float2(-hi.x, -hi.y));
+                        ph[2 * k] = __float_as_uint(hi.x);
+                        ph[2 * k + 1] = __float_as_uint(hi.y);
+                        pl[2 * k] = __float_as_uint(lo.x);
+                        pl[2 * k + 1] = __float_as_uint(lo.y);
                     }
-                    t.x = c0 < nvis && c0 >= nlo ? t.x : -INFINITY;
-                    t.y = c0 + 1 < nvis && c0 + 1 >= nlo ? t.y : -INFINITY;
-                    const float2 e2 = make_float2(ex2(t.x), ex2(t.y));
-                    rs2[k & 3] = fadd2(rs2[k & 3], e2);
-                    ph[2 * k] = __float_as_uint(tf32_hi(e2.x));
-                    ph[2 * k + 1] = __float_as_uint(tf32_hi(e2.y));
-                    pl[2 * k] = __float_as_uint(tf32_lo(e2.x));
-                    pl[2 * k + 1] = __float_as_uint(tf32_lo(e2.y));
+                    tmem_st32(ts + 32 * half, ph);
+                    tmem_st32(tl + C::PL + 32 * half, pl);
                 }
-                tmem_st32(ts + 32 * half, ph);
-                tmem_st32(tl + C::PL + 32 * half, pl);
-            }
+            };
+            if (all_visible && !capped) make_p(false, false);
+            else make_p(!all_visible, capped);
             const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
             const float rs = (r01.x + r01.y) + (r23.x + r23.y);
             l = l * corr + rs;
