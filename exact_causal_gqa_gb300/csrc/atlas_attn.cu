@@ -136,7 +136,7 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
 
     const int G = Hq / Hkv;
     plan->G = G;
-    plan->direct = plan->cluster = 0;
+    plan->direct = plan->cluster = plan->balanced = 0;
     plan->tc_split = 0;
     plan->tiles_per_unit = plan->tiles_per_head = 0;
     if ((int64_t)G * L->q_len > 16) {
@@ -162,6 +162,11 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
             if (chunk > round_up(max_ctx, 128)) chunk = round_up(max_ctx, 128);
             if (tiles > 65535) return ATLAS_ERR_UNSUPPORTED;
             plan->tc_split = 1;
+            // An automatic whole call cuts each sequence into equal splits taken
+            // longest-first (the chunked phases keep fixed chunks: their passes
+            // are defined on them).
+            plan->balanced = L->split_tokens == 0 && L->phase == ATLAS_PHASE_ALL &&
+                             !L->chunk_range && L->batch <= kTcOrderMaxSeqs;
             plan->chunk = (int)chunk;
             plan->n_chunks = (int)((max_ctx + chunk - 1) / chunk);
             const int64_t rows = (int64_t)L->batch * Hq * L->q_len;
@@ -364,6 +369,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         tp.split = plan.tc_split;
         tp.chunk = plan.chunk;
         tp.n_chunks = plan.n_chunks;
+        tp.balanced = plan.balanced;
         tp.require_full = kind == ATLAS_KIND_PREFILL;
         tp.hilo_below = fabsf(scale) * sqrtf((float)D) > kHiLoScale ? INT32_MAX : kHiLoBelow;
         tp.negate_scores = scale < 0.f;
@@ -418,6 +424,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     mp.P = P;
     mp.chunk = plan.chunk;
     mp.n_chunks = plan.n_chunks;
+    mp.balanced = plan.balanced;
     mp.require_full = sp.require_full;
     mp.window = L->window;
     mp.sinks = L->sinks;

@@ -32,6 +32,7 @@
 // lets its copies and MMAs finish, frees TMEM and writes NaN.
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_order.cuh"
 
 #include <math.h>
 
@@ -143,7 +144,18 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     // ------------------------------------------------------------ work item
     const int units = p.B * p.Hkv;
     int u, c, t0, tstep;  // tiles t0 + x * tstep, x < NT
-    if (p.split) {
+    int split_keys = p.chunk;  // keys per split (split mode)
+    if (p.split && p.balanced) {
+        // longest-first work item (the V ring is free until the producer starts)
+        const TcItem it = tc_balanced_item(p, blockIdx.x + blockIdx.y * gridDim.x,
+                                           reinterpret_cast<int *>(smem + C::OFF_V));
+        if (it.b < 0) return;
+        c = it.split;
+        u = it.b * p.Hkv + it.hkv;
+        t0 = it.tile;
+        tstep = 0;
+        split_keys = it.split_keys;
+    } else if (p.split) {
         c = blockIdx.x;
         u = blockIdx.y / p.tiles_per_unit;
         t0 = blockIdx.y % p.tiles_per_unit;
@@ -201,8 +213,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     const int kv_lo = p.window > 0 ? max(0, L - p.q_len + i_min + 1 - p.window) / BN * BN : 0;
     int kv_begin = kv_lo, kv_end = kv_hi;
     if (p.split) {
-        kv_begin = max(c * p.chunk, kv_lo);
-        kv_end = min(kv_hi, c * p.chunk + p.chunk);
+        kv_begin = max(c * split_keys, kv_lo);
+        kv_end = min(kv_hi, c * split_keys + split_keys);
         if (kv_begin >= kv_end) return;
     }
     const int nb = (kv_end - kv_begin + BN - 1) / BN;

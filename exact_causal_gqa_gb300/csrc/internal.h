@@ -18,6 +18,20 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // Keys per pipeline stage of the split-KV kernels.
 constexpr int kSplitBlockTokens = 64;
 
+// Balanced split geometry of the tensor-core path: a context of L keys is cut into
+// n = ceil(L / chunk) splits of round_up(ceil(L / n), 128) keys (the last one
+// shorter), split s covering keys [s * size, (s + 1) * size).  The kernels and the
+// merge derive it from seq_lens alike.
+__host__ __device__ inline int balanced_split(int L, int chunk) {
+    const int Lc = L < 1 ? 1 : L;
+    const int n = (Lc + chunk - 1) / chunk;
+    const int per = (Lc + n - 1) / n;
+    return (per + 127) / 128 * 128;
+}
+// Largest batch whose splits the tensor-core kernels order longest-first (each CTA
+// ranks the batch's sequences itself).
+constexpr int kTcOrderMaxSeqs = 128;
+
 // Everything the split-KV kernels (bf16 mma.sync and f32) and the merge need.
 // "Columns" are the query rows one (sequence, kv head) owns: column n is q head
 // g = n / q_len of the group and query row i = n % q_len.
@@ -58,6 +72,7 @@ struct SplitParams {
 struct MergeParams {
     const int32_t *seq_lens;
     int32_t B, Hq, D, q_len, max_pages, P, chunk, n_chunks, require_full;
+    int32_t balanced;           // splits of balanced_split(seq_len, chunk) keys
     int32_t window;             // splits below a row's window hold nothing for it
     const float *sinks;         // [Hq] natural-log logits or null: one more state (m, 1, 0)
     const int32_t *q_lens;      // [B] ragged query rows or null; padding rows untouched
@@ -81,6 +96,8 @@ struct TcParams {
     int32_t tiles_per_head;   // q_len / 128 when q_len % 128 == 0 (heavy-first order), else 0
     int32_t split;            // 1: write split partials; 0: write the output
     int32_t chunk, n_chunks;  // split geometry (chunk a multiple of 128)
+    int32_t balanced;         // split mode: balanced splits in longest-first order
+                              // (tc_order.cuh); the grid's CTAs are work items
     int32_t require_full;
     int32_t hilo_below;       // tiles whose rows see fewer keys use a hi+lo split of P
     int32_t negate_scores;    // scale < 0: S = -Q K^T with |scale| (keeps the max exact)
@@ -137,6 +154,7 @@ struct Plan {
     Path path;
     int direct;   // bf16 split kernel: one split, output written directly
     int cluster;  // f32 split kernel: splits merged inside one thread-block cluster
+    int balanced; // tensor-core split mode: equal splits per sequence, longest first
     int chunk, n_chunks, col_tiles, G;
     int tc_split, tiles_per_unit, tiles_per_head;
     size_t acc_bytes, ml_offset, ws_bytes;

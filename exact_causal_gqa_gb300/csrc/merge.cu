@@ -38,8 +38,10 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) merge_kernel(const MergePara
     if (!bad_len) {
         const int visible = L - qn + i + 1;
         // splits holding this row's keys: [first, nsplit)
-        const int first = p.window > 0 ? max(0, visible - p.window) / p.chunk : 0;
-        const int nsplit = (visible + p.chunk - 1) / p.chunk;
+        const int chunk =
+            p.balanced ? balanced_split(min(L, p.max_pages * p.P), p.chunk) : p.chunk;
+        const int first = p.window > 0 ? max(0, visible - p.window) / chunk : 0;
+        const int nsplit = (visible + chunk - 1) / chunk;
         const float *ml = p.ws_ml + row * p.n_chunks * 2;
         // A sink is one more state: m = sink * log2(e), l = 1, acc = 0.
         const float sink2 =

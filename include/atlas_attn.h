@@ -204,7 +204,9 @@ size_t atlas_attn_workspace_size(atlas_kind kind, int32_t n_q_heads, int32_t n_k
  * kv head) holds at most 256 KB of K/V; an fp32 call with few query rows whose
  * automatic plan has at most 8 splits, merged inside one thread-block cluster;
  * never with a phase other than ATLAS_PHASE_ALL, a chunk_range or a fixed
- * split_tokens), -1 if the arguments are invalid.  Reads the same fields as
+ * split_tokens), -1 if the arguments are invalid.  An automatic tensor-core plan
+ * with ATLAS_PHASE_ALL cuts each sequence into equal splits of at most this many
+ * keys (fewer for short sequences), taken longest-first.  Reads the same fields as
  * atlas_attn_workspace_size.
  */
 int32_t atlas_attn_split_tokens(atlas_kind kind, int32_t n_q_heads, int32_t n_kv_heads,

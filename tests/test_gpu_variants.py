@@ -30,6 +30,12 @@ PATHS = [
                                                 seed=34), {}),
     ("suffix tensor core", lambda: inputs.make("suffix", 2, 32, 4, 128, 32, [900, 300], q_len=16,
                                                seed=35), dict(split_tokens=256)),
+    # automatic splits: each sequence cut into equal splits, longest first
+    ("suffix tensor core balanced", lambda: inputs.make("suffix", 3, 32, 4, 128, 32,
+                                                        [3000, 300, 1500], q_len=16, seed=27), {}),
+    ("suffix f32 tensor core balanced", lambda: inputs.make("suffix", 3, 16, 2, 64, 32,
+                                                            [3000, 300, 1500], q_len=16,
+                                                            dtype="f32", seed=26), {}),
     ("prefill direct pair", lambda: inputs.make("prefill", 1, 8, 2, 128, 64, [640], seed=36),
      dict(debug_flags=atlas.DEBUG_TC_DIRECT)),
     ("prefill direct single", lambda: inputs.make("prefill", 1, 6, 2, 128, 16, [384], seed=37),
