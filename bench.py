@@ -70,6 +70,9 @@ def parse_args():
                     help="--pool: scratch slots (0: 4096 or two chunks, the larger)")
     ap.add_argument("--append", action="store_true",
                     help="time atlas_kv_append writing the workload's K/V into its pages")
+    ap.add_argument("--settle-s", type=float, default=1.0,
+                    help="untimed steps for this long before the timed region, so that the "
+                         "clock sampler sees the GPU under load (0 for profiler runs)")
     return ap.parse_args()
 
 
@@ -147,7 +150,10 @@ def kernel_source_sha(kernel: str) -> str:
     """Hash of the kernel's translation unit and the headers it shares."""
     csrc = os.path.join(ROOT, "exact_causal_gqa_gb300", "csrc")
     h = hashlib.sha256()
-    for name in (KERNEL_SOURCES[kernel], "ptx.cuh", "internal.h"):
+    names = [KERNEL_SOURCES[kernel], "ptx.cuh", "internal.h"]
+    if kernel.startswith("fmha_"):
+        names.append("tc_order.cuh")
+    for name in names:
         h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
@@ -337,7 +343,7 @@ def measure(args, index, world, rank, local, e2e=True, cpu_budget=12.0):
     with ClockSampler(local) as clocks:
         # Untimed steps for about a second so the clock sampler sees the GPU under
         # this load even when the timed region is shorter than its period.
-        settle_end = time.time() + 1.0
+        settle_end = time.time() + args.settle_s
         while time.time() < settle_end:
             for _ in range(20):
                 step()
