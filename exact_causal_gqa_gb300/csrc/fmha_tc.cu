@@ -100,6 +100,18 @@ struct Cfg {
     }
 };
 
+// As umma_bf16_tmem_a, with the output rows (TMEM lanes) whose bit is set in
+// mask[lane / 32] left unchanged.
+__device__ __forceinline__ void umma_bf16_tmem_a_masked(uint32_t d_tmem, uint32_t a_tmem,
+                                                        uint64_t b_desc, uint32_t idesc,
+                                                        const uint32_t (&mask)[4]) {
+    asm volatile(
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, {%4, %5, %6, %7}, 1;" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(mask[0]), "r"(mask[1]), "r"(mask[2]),
+        "r"(mask[3])
+        : "memory");
+}
+
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort) {
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort, kWaitLimitNs));
 }
@@ -409,17 +421,22 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                     for (int kk = 0; kk < 8; ++kk)
                         umma_bf16_tmem_a(tmem + C::o_col(x), pcol + (kk >> 1) * 32 + (kk & 1) * 8,
                                          vd + kk * 128u, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    // The softmax's vote for this block (written before its P arrival),
-                    // read once the hi products are queued so its latency hides there.
-                    const bool split_blk =
-                        hilo || *reinterpret_cast<volatile uint32_t *>(
-                                    smem + C::OFF_VOTE + (x * 2 + (j & 1)) * 4) != 0u;
-                    if (split_blk) {
+                    // The softmax's vote for this block (one byte per warp, written before
+                    // its P arrival), read once the hi products are queued so its latency
+                    // hides there.  The lo product leaves the rows of warps that did not
+                    // ask for it unchanged: their lo columns hold no P.
+                    const uint32_t vote = *reinterpret_cast<volatile uint32_t *>(
+                        smem + C::OFF_VOTE + (x * 2 + (j & 1)) * 4);
+                    if (hilo || vote != 0u) {
+                        uint32_t off_lanes[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            off_lanes[q] = (hilo || ((vote >> (8 * q)) & 0xffu)) ? 0u : 0xffffffffu;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_bf16_tmem_a(tmem + C::o_col(x),
-                                             pcol + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
-                                             vd + kk * 128u, idPV, 1u);
+                            umma_bf16_tmem_a_masked(tmem + C::o_col(x),
+                                                    pcol + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+                                                    vd + kk * 128u, idPV, off_lanes);
                     }
                     umma_commit(BAR(C::B_PVDONE + x));
                     // Ping-pong: S_x(j + SB) follows PV_x(j) at once, so tile x starts
@@ -554,8 +571,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             const float mref = m_used == -INFINITY ? 0.f : m_used;
             // hi + lo P for this block?  Static per tile; else each warp decides for
             // its 32 rows and leaves its vote for the MMA thread (read after this
-            // warp's P arrival), which multiplies the lo part when any warp of the
-            // tile asked for it.  A warp that did not ask writes zeros there.
+            // warp's P arrival), which multiplies the lo part for the rows of the warps
+            // that asked for it.
             bool split_blk = hilo;
             if (!hilo) {
                 // largest weight maxp = 2^(mx - mref) against w (l corr + maxp), in the
@@ -607,11 +624,6 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                     }
                 }
             };
-            // A warp that did not ask for hi + lo writes zeros over its lo columns, in
-            // case another warp of the tile did (then the MMA multiplies them).
-            uint32_t z16[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) z16[e] = 0u;
             if (!split_blk && all_visible && !capped) {
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
@@ -620,7 +632,6 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                     tmem_wait_ld();
                     quarter(sr, cc, hw, lw, false, false, false);
                     tmem_st16(ts + cc * 32, hw);
-                    if (!hilo) tmem_st16(ts + cc * 32 + 16, z16);
                 }
             } else if (all_visible && !capped) {
 #pragma unroll 1
@@ -640,7 +651,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                     tmem_wait_ld();
                     quarter(sr, cc, hw, lw, !all_visible, split_blk, capped);
                     tmem_st16(ts + cc * 32, hw);
-                    tmem_st16(ts + cc * 32 + 16, split_blk ? lw : z16);
+                    if (split_blk) tmem_st16(ts + cc * 32 + 16, lw);
                 }
             }
             const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
