@@ -608,10 +608,11 @@ def run_pool(args, world, rank, local):
     for _ in range(max(3, args.warmup)):
         _, st = step()
     torch.cuda.synchronize(dev)
-    # the pooled result equals the decode over a fully resident pool, bit for bit
+    # the pooled result equals the decode over a fully resident pool with the same
+    # split size, bit for bit
     resident = inputs.Problem(**{k: (v.to(dev) if torch.is_tensor(v) else v)
                                  for k, v in vars(host).items()})
-    ref = atlas.run(resident, out_dtype=out_dtype)
+    ref = atlas.run(resident, out_dtype=out_dtype, split_tokens=chunk)
     torch.cuda.synchronize(dev)
     bitwise = bool(torch.equal(out, ref))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -141,6 +141,7 @@ template <int NT, int D>
 __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+    allow_dependent_launch();  // the merge may start its CTAs (it waits for this grid)
     using C = Cfg<NT, D>;
     constexpr int S = C::kStages, SB = C::kSB;
     constexpr int kTileBytes = C::kTileBytes;

@@ -169,6 +169,7 @@ template <int D>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
     fmha_tf32x3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+    allow_dependent_launch();  // the merge may start its CTAs (it waits for this grid)
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];

@@ -6,6 +6,9 @@
 //   lse = ln 2 * (M + log2 sum_s w_s l_s).
 // One warp per row; lanes split the head dimension (float4 / float2 loads).
 // S is derived on the device from seq_lens, so no host sync is needed.
+// Launched as a programmatic dependent of the split kernel before it: its CTAs
+// may start while that kernel's last CTAs still run, read their sequence's
+// length, and wait (griddepcontrol.wait) before the first partial is read.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -31,6 +34,8 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) merge_kernel(const MergePara
     const bool bad_len = qn < 0 || qn > p.q_len || L < qn || L > p.max_pages * p.P ||
                          (p.require_full && L != qn);
     if (!bad_len && i >= qn) return;  // padding row: not a query, not written
+    // the split kernel that wrote the partials has completed, its writes visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     float o[DPL];
     float lse = __int_as_float(0x7fc00000);
@@ -132,10 +137,17 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) merge_kernel(const MergePara
 
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream) {
     const int64_t rows = (int64_t)p.B * p.Hq * p.q_len;
-    const unsigned grid = (unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta);
-    if (p.D == 128) merge_kernel<128><<<grid, kRowsPerCta * 32, 0, stream>>>(p);
-    else merge_kernel<64><<<grid, kRowsPerCta * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta), 1, 1);
+    cfg.blockDim = dim3(kRowsPerCta * 32, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return p.D == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<128>, p)
+                      : cudaLaunchKernelEx(&cfg, merge_kernel<64>, p);
 }
 
 }  // namespace atlas

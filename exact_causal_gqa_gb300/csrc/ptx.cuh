@@ -85,6 +85,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Let the next kernel in the stream, launched as a programmatic dependent (the
+// merge), start its CTAs once every CTA of this grid has executed this; it still
+// waits for this grid to complete before it reads what this grid writes.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy; with src_bytes = 0 the destination is zero-filled
 // and nothing is read.

@@ -273,6 +273,7 @@ template <int D, int NT, int STAGES>
 __global__ void __launch_bounds__(kSplitThreads, 2)
     split_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    allow_dependent_launch();  // the merge may start its CTAs (it waits for this grid)
     using Lay = SplitLayout<D, NT, STAGES>;
     constexpr int NCOLS = NT * 8;
     constexpr int KSTEPS = D / 16;
@@ -706,6 +707,7 @@ struct F32Layout {
 template <int D, int NC>
 __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kMinCtas)
     split_f32_kernel(const SplitParams p) {
+    allow_dependent_launch();  // the merge may start its CTAs (it waits for this grid)
     using Lay = F32Layout<D, NC>;
     constexpr int W = Lay::W, BK = kF32Keys, DPL = D / 32, NQ = NC / 4, DV4 = D / 4;
     extern __shared__ __align__(16) float f32d_smem[];

@@ -131,7 +131,7 @@ typedef struct {
      * atlas_pool.h serves a context larger than its device slots this way): the
      * split-KV chunks go to the same workspace pass by pass, then one merge reads
      * them all.  Each chunk's partial state depends only on its keys, so the
-     * result is bit-identical to a single launch with the same sizes. */
+     * result is bit-identical to a single launch with the same sizes and split_tokens. */
     const int32_t *chunk_range; /* optional device [batch][2]: compute only chunks s with
                                    chunk_range[b][0] <= s < chunk_range[b][1] of sequence b
                                    (chunks of atlas_attn_split_tokens keys, from key 0);

@@ -118,10 +118,17 @@ def test_pooled_decode_matches_the_oracle_with_automatic_splits():
 
 def test_pooled_decode_on_the_tensor_core_path():
     # G = 32 query heads per kv head: the decode takes the tcgen05 path, whose
-    # chunked form the passes use.
+    # chunked form the passes use.  The passes keep fixed chunks (their split size
+    # for the chunked phases); a resident call with that split size gives the same
+    # bits (an automatic resident call cuts each sequence into equal splits instead,
+    # equal within the tolerance, not bitwise).
     prob = host_problem(B=2, Hq=32, Hkv=1, lens=(3000, 1500), seed=3)
     dev = to_device(prob)
-    ref = atlas.run(dev, out_dtype=torch.float32)
+    chunk = atlas.split_tokens_of("decode", dev.q.shape, prob.n_q_heads, prob.n_kv_heads,
+                                  prob.head_dim, prob.page_tokens, prob.max_pages,
+                                  prob.num_pages, dev.q.dtype, torch.float32,
+                                  phase=atlas.PHASE_CHUNKS)
+    ref = atlas.run(dev, out_dtype=torch.float32, split_tokens=chunk)
     pool = atlas.HotPagePool(pinned(prob.k_pages), pinned(prob.v_pages), hot_slots=16,
                              scratch_slots=80)
     out, st = pool.decode(dev.q, prob.page_table, prob.seq_lens, prob.n_q_heads, prob.scale,
