@@ -604,7 +604,7 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
 
 template <int NCOLS, int D>
 __device__ void cluster_merge(const SplitParams &p, const float *part, int col0, int ncols,
-                              int qn, bool bad_len) {
+                              int qn, bool bad_len, int seq_len) {
     constexpr int kMaxSplits = 8;  // the portable cluster size
     __syncthreads();
     cluster_barrier();  // every split's state is in its CTA's shared memory
@@ -613,7 +613,7 @@ __device__ void cluster_merge(const SplitParams &p, const float *part, int col0,
         // each element's loads from all splits are issued before any is used.
         const int b = blockIdx.z;
         const int hkv = blockIdx.y / p.col_tiles;
-        const int L = p.seq_lens[b];
+        const int L = seq_len;  // seq_lens[b], read at the kernel's start
         const uint32_t base = smem_u32(part);
         const int rank = (int)cluster_ctarank();
         for (int idx = rank * (int)blockDim.x + (int)threadIdx.x; idx < ncols * D;
@@ -715,33 +715,48 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
     float *sW = sQ + Lay::kQ;
     float *part = sW + W * Lay::kWarp;  // cluster mode only
 
+    const int b = blockIdx.z;
+    const int hkv = blockIdx.y / p.col_tiles;
+    // A short call is a chain of dependent memory round trips, so the reads that do
+    // not depend on seq_len start now, before the prologue waits for it: the CTA's
+    // query rows (cp.async; columns past the tile's end are zero-filled, padding rows
+    // of a ragged batch load too and are masked with their keys) and, into L2, the
+    // page-table entries of this split.
+    const int seq_len_b = p.seq_lens[b];
+    {
+        const int c0 = (int)(blockIdx.y % p.col_tiles) * NC;
+        const int nc = min(NC, p.G * p.q_len - c0);
+        for (int idx = threadIdx.x; idx < NC * DV4; idx += W * 32) {
+            const int c = idx / DV4, d4 = idx % DV4;
+            const bool in = c < nc;
+            const float *src = static_cast<const float *>(p.q) +
+                               column_row(p, b, hkv, c0 + (in ? c : 0)) * D + 4 * d4;
+            cp_async16(smem_u32(sQ + c * Lay::KS + 4 * d4), src, in ? 16u : 0u);
+        }
+        cp_async_commit();
+        const int pg0 = (int)blockIdx.x * p.chunk / p.P;
+        const int npg = min(p.chunk / p.P, p.max_pages - pg0);
+        if ((int)threadIdx.x * 32 < npg)
+            prefetch_l2(p.page_table + (int64_t)b * p.max_pages + pg0 + threadIdx.x * 32);
+    }
     int L = 0, kv_begin = 0, kv_end = 0, col0 = 0, ncols = 0, qn = 0, why = 0;
     const bool work = split_prologue<NC>(p, blockIdx.y % p.col_tiles, L, kv_begin, kv_end, col0,
                                          ncols, qn, why);
+    if (!work) cp_async_wait<0>();  // no copy in flight when the CTA leaves
     if (!work && !p.cluster) return;
     if (!work) {
         // an empty state (m = -inf, l = 0, acc = 0), or NaN after a bad page id
         const float nan = __int_as_float(0x7fc00000);
         for (int idx = threadIdx.x; idx < NC * (D + 2); idx += W * 32)
             part[idx] = why == kBadPage ? nan : (idx % (D + 2) == D ? -INFINITY : 0.f);
-        cluster_merge<NC, D>(p, part, col0, ncols, qn, why == kBadLen);
+        cluster_merge<NC, D>(p, part, col0, ncols, qn, why == kBadLen, seq_len_b);
         return;
     }
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int b = blockIdx.z;
-    const int hkv = blockIdx.y / p.col_tiles;
     const float *kp = static_cast<const float *>(p.k_pages);
     const float *vp = static_cast<const float *>(p.v_pages);
     const int32_t *ptab = p.page_table + (int64_t)b * p.max_pages;
 
-    for (int idx = threadIdx.x; idx < NC * DV4; idx += W * 32) {
-        const int c = idx / DV4, d4 = idx % DV4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < ncols && (col0 + c) % p.q_len < qn)
-            v = reinterpret_cast<const float4 *>(static_cast<const float *>(p.q) +
-                                                 column_row(p, b, hkv, col0 + c) * D)[d4];
-        *reinterpret_cast<float4 *>(sQ + c * Lay::KS + 4 * d4) = v;
-    }
     int lim[NC], lo[NC];
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -749,7 +764,6 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
         lim[c] = ok ? min(kv_end, column_visible(p, L, col0 + c)) : kv_begin;
         lo[c] = ok ? column_first(p, L, col0 + c) : 0;
     }
-    __syncthreads();
 
     float *wK = sW + warp * Lay::kWarp;
     float *wV = wK + 2 * Lay::kBuf;
@@ -792,6 +806,8 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
     int j = warp;
     if (j < nblk) load(kv_begin + j * BK, 0);
     cp_async_commit();
+    cp_async_wait<1>();  // the query rows (the group before this one) have landed
+    __syncthreads();     // ... and every warp sees them
     for (int it = 0; j < nblk; ++it, j += W) {
         const int kb = kv_begin + j * BK;
         const int buf = it & 1;
@@ -914,7 +930,7 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
     __syncthreads();
     if (p.cluster) {
         write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, qn, false, part);
-        cluster_merge<NC, D>(p, part, col0, ncols, qn, false);
+        cluster_merge<NC, D>(p, part, col0, ncols, qn, false, seq_len_b);
         return;
     }
     write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, qn, false);
