@@ -115,3 +115,39 @@ def test_ragged_batches(kind, B, Hq, Hkv, P, q_len, lens, q_lens, kw):
     for b in range(B):
         np.testing.assert_allclose(lse_h[b, :, :q_lens[b]], ref_lse[b, :, :q_lens[b]],
                                    rtol=0, atol=1e-4)
+
+
+RAGGED_F32 = [
+    # (B, Hq, Hkv, D, P, q_len, seq_lens, q_lens, call kwargs): the fp32 split kernel, whose
+    # CTAs load their query rows before seq_len and q_lens are known
+    (2, 8, 2, 128, 16, 3, [400, 90], [2, 3], {}),                      # cluster merge
+    (2, 8, 2, 128, 16, 3, [400, 90], [2, 1], dict(split_tokens=64)),   # splits + merge kernel
+    (3, 8, 4, 64, 16, 2, [300, 77, 500], [1, 2, 0], {}),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,q_len,lens,q_lens,kw", RAGGED_F32)
+def test_ragged_f32_with_poisoned_padding_rows(B, Hq, Hkv, D, P, q_len, lens, q_lens, kw):
+    prob = inputs.make("suffix", B, Hq, Hkv, D, P, lens, q_len=q_len, dtype="f32",
+                       seed=90 + q_len)
+    for b in range(B):  # padding query rows hold NaN: masked if read, never written
+        prob.q[b, :, q_lens[b]:, :] = float("nan")
+    ref, ref_lse = oracle_rows(prob, want_lse=True, q_lens=np.int32(q_lens))
+    dev = prob.to(DEV)
+    ql = torch.tensor(q_lens, dtype=torch.int32, device=DEV)
+    sentinel = 12345.0
+    out = torch.full(prob.q.shape, sentinel, dtype=torch.float32, device=DEV)
+    lse = torch.full((flat_rows(prob),), sentinel, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    run_gpu(dev, out=out, out_dtype=torch.float32, lse=lse, status=status, q_lens=ql, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.cpu()
+    lse_h = lse.cpu().numpy().reshape(B, Hq, q_len)
+    for b in range(B):
+        qn = q_lens[b]
+        if qn:
+            assert_parity(prob, got[b, :, :qn], ref[b, :, :qn], f"f32 ragged seq {b}")
+            np.testing.assert_allclose(lse_h[b, :, :qn], ref_lse[b, :, :qn], rtol=0, atol=2e-5)
+        assert torch.all(got[b, :, qn:] == sentinel)
+        assert np.all(lse_h[b, :, qn:] == sentinel)
