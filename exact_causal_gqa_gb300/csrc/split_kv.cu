@@ -904,7 +904,7 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
 #pragma unroll
                 for (int e = 0; e < DPL; ++e) acc[c][e] = fmaf(pk[c], vv[e], acc[c][e]);
         }
-        __syncwarp();  // P and this buffer are rewritten by the next round
+        __syncwarp();  // P and this buffer are rewritten by the next iteration
     }
     cp_async_wait<0>();
 #pragma unroll
