@@ -200,3 +200,23 @@ def test_late_score_jumps(kind, q_len, lens):
     prob = inputs.make(kind, len(lens), 8, 2, 128, 64, lens, q_len=q_len, seed=21,
                        k_outlier_prob=0.002, k_outlier_scale=16.0)
     check(prob)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_suffix_batch_past_the_longest_first_order(dtype):
+    """More sequences than the kernels order longest-first (kTcOrderMaxSeqs = 128): the
+    automatic plan falls back to fixed chunks in grid order, with split + merge."""
+    B = 131
+    g = np.random.default_rng(5)
+    lens = [int(x) for x in g.integers(20, 2500, size=B)]
+    prob = inputs.make("suffix", B, 8, 1, 64, 32, lens, q_len=4, dtype=dtype, seed=41)
+    ref, ref_lse = oracle_rows(prob, want_lse=True)
+    dev = prob.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lse = torch.empty(flat_rows(prob), dtype=torch.float32, device=DEV)
+    out = run_gpu(dev, out_dtype=torch.float32, lse=lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_parity(prob, out, ref, f"B{B} {dtype}")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.reshape(-1), rtol=0,
+                               atol=2e-4 if dtype == "bf16" else 2e-5)
