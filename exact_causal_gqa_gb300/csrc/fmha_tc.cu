@@ -645,14 +645,27 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                     tmem_st16(ts + cc * 32 + 16, lw);
                 }
             } else {
+                // Masked (a diagonal or window block) or soft-capped: each combination of
+                // the flags gets its own loop, so that no pair computes what a branch not
+                // taken would need (the caps' tanh in particular).
+                auto general = [&](const bool masked, const bool split, const bool cap) {
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t sr[32], hw[16], lw[16];
-                    tmem_ld32(ts + cc * 32, sr);
-                    tmem_wait_ld();
-                    quarter(sr, cc, hw, lw, !all_visible, split_blk, capped);
-                    tmem_st16(ts + cc * 32, hw);
-                    if (split_blk) tmem_st16(ts + cc * 32 + 16, lw);
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t sr[32], hw[16], lw[16];
+                        tmem_ld32(ts + cc * 32, sr);
+                        tmem_wait_ld32(sr);
+                        quarter(sr, cc, hw, lw, masked, split, cap);
+                        tmem_st16(ts + cc * 32, hw);
+                        if (split) tmem_st16(ts + cc * 32 + 16, lw);
+                    }
+                };
+                if (capped) {
+                    if (split_blk) general(!all_visible, true, true);
+                    else general(!all_visible, false, true);
+                } else if (split_blk) {
+                    general(true, true, false);
+                } else {
+                    general(true, false, false);
                 }
             }
             const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
