@@ -512,6 +512,23 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             // Padding rows of a ragged batch never reach the output: they may take the
             // unmasked path (their O and l are garbage but stay in their own row).
             const bool all_visible = __all_sync(0xffffffffu, !valid || (nvis >= BN && nlo <= 0));
+            // A masked block, quarter by quarter (32 keys), for all the warp's real rows:
+            // wholly masked (bit in q_none: nothing loaded, P = 0), wholly visible (bit in
+            // q_full: the unmasked code), or mixed.  On the causal diagonal the quarters
+            // before a warp's own rows are visible and those after them masked.
+            int q_full = 0, q_none = 0;
+            if (!all_visible) {
+                const int hi = min(max(nvis, 0), BN), lo = min(max(nlo, 0), BN);
+                const int hi_min = __reduce_min_sync(0xffffffffu, valid ? hi : BN);
+                const int hi_max = __reduce_max_sync(0xffffffffu, valid ? hi : 0);
+                const int lo_min = __reduce_min_sync(0xffffffffu, valid ? lo : BN);
+                const int lo_max = __reduce_max_sync(0xffffffffu, valid ? lo : 0);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    if (32 * cc >= hi_max || 32 * cc + 32 <= lo_min) q_none |= 1 << cc;
+                    else if (32 * cc >= lo_max && 32 * cc + 32 <= hi_min) q_full |= 1 << cc;
+                }
+            }
             // Pass 1: row max of the raw scores (scale_log2 >= 0, so the scaled
             // maximum is the maximum scaled), four chains of 3-input max.
             // Outer loops stay rolled: a fully unrolled body overflows the
@@ -542,9 +559,14 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             } else {
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
+                    if ((q_none >> cc) & 1) continue;
                     uint32_t sr[32];
                     tmem_ld32(ts + cc * 32, sr);
-                    tmem_wait_ld();
+                    tmem_wait_ld32(sr);
+                    if ((q_full >> cc) & 1) {
+                        max32(sr);
+                        continue;
+                    }
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         const int col = cc * 32 + e;
@@ -659,13 +681,33 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                         if (split) tmem_st16(ts + cc * 32 + 16, lw);
                     }
                 };
+                // Masked, uncapped: quarter by quarter as classified above.
+                auto masked_blk = [&](const bool split) {
+#pragma unroll 1
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t sr[32], hw[16], lw[16];
+                        if ((q_none >> cc) & 1) {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) hw[k] = 0u;
+                            tmem_st16(ts + cc * 32, hw);
+                            if (split) tmem_st16(ts + cc * 32 + 16, hw);
+                            continue;
+                        }
+                        tmem_ld32(ts + cc * 32, sr);
+                        tmem_wait_ld32(sr);
+                        if ((q_full >> cc) & 1) quarter(sr, cc, hw, lw, false, split, false);
+                        else quarter(sr, cc, hw, lw, true, split, false);
+                        tmem_st16(ts + cc * 32, hw);
+                        if (split) tmem_st16(ts + cc * 32 + 16, lw);
+                    }
+                };
                 if (capped) {
                     if (split_blk) general(!all_visible, true, true);
                     else general(!all_visible, false, true);
                 } else if (split_blk) {
-                    general(true, true, false);
+                    masked_blk(true);
                 } else {
-                    general(true, false, false);
+                    masked_blk(false);
                 }
             }
             const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
