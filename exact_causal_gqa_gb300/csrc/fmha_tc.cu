@@ -60,7 +60,7 @@ struct Cfg {
     // K/V ring depth: the same bytes in flight for either head_dim
     static constexpr int kStages = (NT == 2 ? 2 : 3) * (128 / D);
     static constexpr int kSB = NT == 2 ? 1 : 2;      // S buffers per tile
-    // warps 0-2: producer, MMA issuer, tail fix-up (warp 3 idle); then NT softmax
+    // warps 0-3: K producer (and Q), MMA issuer, tail fix-up, V producer; then NT softmax
     // warpgroups.  Each SMSP holds 16K registers and 3 of the 12 warps (NT = 2):
     // 168 registers per thread.
     static constexpr int kSoftmaxWarp0 = 4;
@@ -286,14 +286,17 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     bool failed = false;
 
-    if (warp == 0) {
-        // -------------------------------------------------------- TMA producer
-        // The whole warp walks the blocks (page ids come from a warp-wide cache);
-        // lane 0 issues the copies.
-        if (lane == 0) {
+    if (warp == 0 || warp == 3) {
+        // -------------------------------------------------------- TMA producers
+        // Warp 0 streams Q and the K ring, warp 3 the V ring, each through its own
+        // warp-wide page-id cache.  A block starts on a multiple of 128 keys and P (a
+        // power of two <= 128) divides that, so box bx of a block is page
+        // kb / P + bx from its first row, and a block's pages lie in one 32-page line
+        // of the cache: lane bx looks its page up with one shuffle and issues box bx.
+        const int kv = warp == 0 ? 0 : 1;
+        if (kv == 0 && lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
             mbar_arrive_expect_tx(BAR(C::B_Q), NT * kTileBytes);
             for (int x = 0; x < NT; ++x) {
                 const int qrow = (int)tile_row(p, b, hkv, (t0 + x * tstep) * BM);
@@ -303,52 +306,42 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                                 BAR(C::B_Q));
             }
         }
-        PageIdCache pages{p.page_table + (int64_t)b * p.max_pages, (kv_end - 1) / p.P};
-        const int BR = p.P < BN ? p.P : BN;
-        int issued_k = 0, issued_v = 0;
-        for (int j = 0; j < nb && !failed; ++j) {
+        if (kv == 1 && lane == 0) prefetch_tmap(&tmV);
+        const CUtensorMap *map = kv == 0 ? &tmK : &tmV;
+        const uint32_t ring = sb + (kv == 0 ? C::OFF_K : C::OFF_V);
+        const int bar_full = kv == 0 ? C::B_KFULL : C::B_VFULL;
+        const int bar_empty = kv == 0 ? C::B_KEMPTY : C::B_VEMPTY;
+        const int lp = 31 - __clz(p.P);  // log2(P)
+        PageIdCache pages{p.page_table + (int64_t)b * p.max_pages, (kv_end - 1) >> lp};
+        int issued = 0;
+        for (int j = 0; j < nb; ++j) {
             const int s = j % S, use = j / S;
             const int kb = kv_begin + j * BN;
-            const int ke = min(kb + BN, kv_end);
-            const int nbox = (ke - kb + BR - 1) / BR;
-            const uint32_t bytes = (uint32_t)(nbox * BR * 128 * C::kSlabs);
-            // y coordinate of box bx of this block (lane bx holds it; nbox <= 16)
-            int my_y = 0;
-            for (int bx = 0; bx < nbox; ++bx) {
-                const int tk = kb + bx * BR;
-                const int y = (pages.get(tk / p.P) * p.Hkv + hkv) * p.P + (tk % p.P);
-                if (lane == bx) my_y = y;
+            const int nbox = (min(BN, kv_end - kb) + p.P - 1) >> lp;  // <= 16
+            const int y = (pages.get_line(kb >> lp, lane < nbox ? lane : 0) * p.Hkv + hkv) << lp;
+            if (use > 0 && !wait_warp(BAR(bar_empty + s), (use - 1) & 1, abort_flag)) {
+                failed = true;
+                break;
             }
-            for (int kv = 0; kv < 2; ++kv) {
-                const int full = (kv == 0 ? C::B_KFULL : C::B_VFULL) + s;
-                const int empty = (kv == 0 ? C::B_KEMPTY : C::B_VEMPTY) + s;
-                if (use > 0 && !wait_warp(BAR(empty), (use - 1) & 1, abort_flag)) {
-                    failed = true;
-                    break;
-                }
-                if (lane < nbox) {
-                    const CUtensorMap *map = kv == 0 ? &tmK : &tmV;
-                    const uint32_t dst = sb + (kv == 0 ? C::OFF_K : C::OFF_V) + s * kTileBytes;
-                    if (lane == 0) mbar_arrive_expect_tx(BAR(full), bytes);
-                    __syncwarp((1u << nbox) - 1u);
+            if (lane < nbox) {
+                if (lane == 0)
+                    mbar_arrive_expect_tx(BAR(bar_full + s),
+                                          (uint32_t)(nbox << lp) * 128u * C::kSlabs);
+                __syncwarp((1u << nbox) - 1u);
 #pragma unroll
-                    for (int sl = 0; sl < C::kSlabs; ++sl)
-                        tma_load_2d(dst + sl * kSlab + lane * BR * 128, map, 64 * sl, my_y,
-                                    BAR(full));
-                }
-                __syncwarp();
-                if (kv == 0) issued_k = j + 1;
-                else issued_v = j + 1;
+                for (int sl = 0; sl < C::kSlabs; ++sl)
+                    tma_load_2d(ring + s * kTileBytes + sl * kSlab + (lane << lp) * 128, map,
+                                64 * sl, y, BAR(bar_full + s));
             }
+            __syncwarp();
+            issued = j + 1;
         }
         if (failed && lane == 0) {
             *abort_flag = 1;
             int no_abort = 0;
-            mbar_wait_bounded(BAR(C::B_Q), 0, &no_abort, kWaitLimitNs);
-            for (int j = max(0, issued_k - S); j < issued_k; ++j)
-                mbar_wait_bounded(BAR(C::B_KFULL + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
-            for (int j = max(0, issued_v - S); j < issued_v; ++j)
-                mbar_wait_bounded(BAR(C::B_VFULL + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
+            if (kv == 0) mbar_wait_bounded(BAR(C::B_Q), 0, &no_abort, kWaitLimitNs);
+            for (int j = max(0, issued - S); j < issued; ++j)
+                mbar_wait_bounded(BAR(bar_full + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -440,6 +433,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                                                     vd + kk * 128u, idPV, off_lanes);
                     }
                     umma_commit(BAR(C::B_PVDONE + x));
+                    // The V stage is free once the last tile's PV has read it: release
+                    // it before S_x(j + SB) waits for its K block.
+                    if (x == NT - 1) umma_commit(BAR(C::B_VEMPTY + s));
                     // Ping-pong: S_x(j + SB) follows PV_x(j) at once, so tile x starts
                     // its next softmax while the other tile's P is still being made.
                     // It writes the S buffer that PV_x(j) reads P_x(j) from; the
@@ -451,7 +447,6 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit(BAR(C::B_VEMPTY + s));
             }
             if (!ok) {
                 failed = true;

@@ -174,6 +174,17 @@ struct PageIdCache {
         }
         return __shfl_sync(0xffffffffu, mine, pg - nb);
     }
+    // Page id of logical page pg0 + i, for a pg0 that every lane passes alike and
+    // pg0 % 32 + i < 32: one line serves the lanes' different pages.
+    __device__ __forceinline__ int get_line(int pg0, int i) {
+        const int lane = threadIdx.x & 31;
+        const int nb = pg0 & ~31;
+        if (nb != base) {
+            base = nb;
+            mine = (nb + lane <= last) ? row[nb + lane] : 0;
+        }
+        return __shfl_sync(0xffffffffu, mine, pg0 - nb + i);
+    }
 };
 
 // ---------------------------------------------------------------- mma.sync path
