@@ -128,6 +128,8 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         L->window > 0 ? std::min(max_ctx, (int64_t)L->window + L->q_len + 127) : max_ctx;
     if ((int64_t)L->num_pages * Hkv * P >= INT32_MAX) return ATLAS_ERR_INVALID_ARG;
     if (L->q_len > max_ctx) return ATLAS_ERR_INVALID_ARG;
+    // Output rows are indexed in 32 bits (the merge, the tensor-core tiles).
+    if ((int64_t)L->batch * Hq * L->q_len >= INT32_MAX) return ATLAS_ERR_INVALID_ARG;
     if (L->split_tokens < 0 || L->split_tokens % kSplitBlockTokens != 0)
         return ATLAS_ERR_INVALID_ARG;
     if (L->phase != ATLAS_PHASE_ALL && L->phase != ATLAS_PHASE_CHUNKS &&
@@ -145,7 +147,6 @@ atlas_status make_plan(atlas_kind kind, int32_t Hq, int32_t Hkv, int32_t D, int3
         plan->path = L->kv_dtype == ATLAS_BF16 ? Path::TensorCore : Path::TensorCoreF32;
         const int64_t tiles_per_unit = ((int64_t)G * L->q_len + 127) / 128;
         const int64_t tiles = (int64_t)L->batch * Hkv * tiles_per_unit;
-        if ((int64_t)L->batch * Hq * L->q_len >= INT32_MAX) return ATLAS_ERR_INVALID_ARG;
         plan->tiles_per_unit = (int)tiles_per_unit;
         plan->col_tiles = 0;
         int64_t chunk = 0;

@@ -753,47 +753,62 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 l = l * osc + ex2(sink2 - M);
                 m_used = M;
             }
-            const float inv = osc / l;
+            const float inv = p.split ? 1.f : osc / l;
             const int64_t slot = row * p.n_chunks + c;
+            // The warp's 32 rows go through shared memory so that each global store
+            // instruction writes whole rows: lane r holds row r of the warp, whose
+            // 16-byte chunk c sits at chunk c ^ (r & 7) of its staging row, so that
+            // both the row-wise writes and the chunk-wise reads are free of bank
+            // conflicts.  Every MMA that reads shared memory has completed by now except
+            // the other tile's last PV, whose V stage and P lie outside this tile's
+            // staging area (tile 0: the Q tiles; tile 1: the V stages, written once its
+            // own PV is done).
+            const bool wide = p.split || !p.out_bf16;  // fp32 rows, else bf16 rows
+            const int rb = wide ? D * 4 : D * 2;       // bytes per output row
+            const uint32_t stage = sb + (uint32_t)(x * 4 + q4) * (32u * D * 4u);
+            const uint32_t my_row = stage + (uint32_t)lane * rb;
 #pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
                 tmem_ld32(to + cc * 32, o);
                 tmem_wait_ld();
-                if (!valid) continue;
-                if (p.split) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + slot * D + cc * 32);
+                if (wide) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                             __uint_as_float(o[4 * k + 2]),
-                                             __uint_as_float(o[4 * k + 3]));
-                } else if (p.out_bf16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                           row * D + cc * 32);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(o[8 * k + 0]) * inv,
-                                        __uint_as_float(o[8 * k + 1]) * inv);
-                        v.y = pack_bf16(__uint_as_float(o[8 * k + 2]) * inv,
-                                        __uint_as_float(o[8 * k + 3]) * inv);
-                        v.z = pack_bf16(__uint_as_float(o[8 * k + 4]) * inv,
-                                        __uint_as_float(o[8 * k + 5]) * inv);
-                        v.w = pack_bf16(__uint_as_float(o[8 * k + 6]) * inv,
-                                        __uint_as_float(o[8 * k + 7]) * inv);
-                        dst[k] = v;
-                    }
+                        st_shared_v4(my_row + (uint32_t)(((cc * 8 + k) ^ (lane & 7)) * 16),
+                                     __float_as_uint(__uint_as_float(o[4 * k]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * k + 1]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * k + 2]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * k + 3]) * inv));
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
-                                                             row * D + cc * 32);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv,
-                                             __uint_as_float(o[4 * k + 1]) * inv,
-                                             __uint_as_float(o[4 * k + 2]) * inv,
-                                             __uint_as_float(o[4 * k + 3]) * inv);
+                    for (int k = 0; k < 4; ++k)
+                        st_shared_v4(my_row + (uint32_t)(((cc * 4 + k) ^ (lane & 7)) * 16),
+                                     pack_bf16(__uint_as_float(o[8 * k + 0]) * inv,
+                                               __uint_as_float(o[8 * k + 1]) * inv),
+                                     pack_bf16(__uint_as_float(o[8 * k + 2]) * inv,
+                                               __uint_as_float(o[8 * k + 3]) * inv),
+                                     pack_bf16(__uint_as_float(o[8 * k + 4]) * inv,
+                                               __uint_as_float(o[8 * k + 5]) * inv),
+                                     pack_bf16(__uint_as_float(o[8 * k + 6]) * inv,
+                                               __uint_as_float(o[8 * k + 7]) * inv));
                 }
+            }
+            __syncwarp();
+            // Byte offset of this thread's row in its destination, -1 for a row that
+            // is not written.
+            uint8_t *const dst_base = p.split ? reinterpret_cast<uint8_t *>(p.ws_acc)
+                                              : static_cast<uint8_t *>(p.out);
+            const int64_t my_off = !valid ? -1 : (p.split ? slot : row) * (int64_t)rb;
+            const int cpr = rb / 16;       // 16-byte chunks per row: 8, 16 or 32
+            const int rpi = 32 / cpr;      // rows per store instruction
+            const int ch = lane % cpr;     // this lane's chunk of its row
+#pragma unroll 1
+            for (int r0 = 0; r0 < 32; r0 += rpi) {
+                const int r = r0 + lane / cpr;
+                const int64_t off = __shfl_sync(0xffffffffu, my_off, r);
+                const uint4 v = ld_shared_v4(stage + (uint32_t)(r * rb + ((ch ^ (r & 7)) * 16)));
+                if (off >= 0) *reinterpret_cast<uint4 *>(dst_base + off + ch * 16) = v;
             }
             if (valid) {
                 if (p.split) {

@@ -97,7 +97,8 @@ typedef struct {
     int32_t batch;             /* B >= 1 */
     int32_t max_pages_per_seq; /* page_table row length */
     int32_t num_pages;         /* pages in each pool */
-    int32_t q_len;             /* 1 for decode, SQ for suffix, S for prefill */
+    int32_t q_len;             /* 1 for decode, SQ for suffix, S for prefill;
+                                  batch * n_q_heads * q_len < 2^31 - 1 */
     atlas_dtype q_dtype;       /* must equal kv_dtype */
     atlas_dtype kv_dtype;
     atlas_dtype out_dtype;

@@ -91,6 +91,7 @@ def test_workspace_size_matches_the_split_layout(lib):
     (dict(split_tokens=100), SIZE_MAX),     # splits must be multiples of 64
     (dict(out_dtype=0, q_dtype=0, kv_dtype=1), SIZE_MAX),  # q and K/V dtypes differ
     (dict(kv_dtype=0, q_dtype=0, out_dtype=1), SIZE_MAX),  # f32 K/V only gives f32 out
+    (dict(batch=1 << 23, Hq=256), SIZE_MAX),  # batch * n_q_heads * q_len >= 2^31 - 1
 ])
 def test_invalid_plans_are_rejected(lib, kw, expect):
     assert ws(lib, **kw) == expect
