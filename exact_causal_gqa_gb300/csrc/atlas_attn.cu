@@ -435,6 +435,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
     mp.out = L->out;
     mp.out_bf16 = L->out_dtype == ATLAS_BF16;
     mp.lse = L->lse;
+    mp.sms = L->sm_count > 0 ? L->sm_count : device_sm_count();
     err = launch_merge(mp, stream);
     if (err != cudaSuccess) return ATLAS_ERR_CUDA;
     if (ev[2] && cudaEventRecord(ev[2], stream) != cudaSuccess) return ATLAS_ERR_CUDA;

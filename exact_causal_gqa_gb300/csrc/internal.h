@@ -81,6 +81,8 @@ struct MergeParams {
     void *out;
     int32_t out_bf16;
     float *lse;
+    int32_t sms;            // SM count: sizes the warps per row
+    int32_t warps_per_row;  // set by launch_merge
 };
 
 // Tensor-core (tcgen05 / TMEM) path for many query rows per (sequence, kv head):

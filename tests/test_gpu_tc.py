@@ -122,6 +122,21 @@ def test_tc_bad_page_and_seq_len(flags, split):
     assert torch.isfinite(out[0]).all()
 
 
+@pytest.mark.parametrize("flags", [atlas.DEBUG_TC_DIRECT, 0])
+@pytest.mark.parametrize("bad", ["negative", "num_pages", "huge"])
+def test_prefill_bad_page_id_poisons_the_rows_that_read_it(bad, flags):
+    # page 3 of sequence 0 holds keys 192..255: rows from 192 on read it, rows below
+    # 128 sit in tiles whose key range ends before it
+    prob = inputs.make("prefill", 2, 8, 2, 128, 64, [384, 384], seed=6)
+    prob.page_table[0, 3] = {"negative": -1, "num_pages": prob.num_pages, "huge": 1 << 30}[bad]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, status=status, debug_flags=flags)
+    torch.cuda.synchronize()
+    assert int(status.item()) == atlas.DEV_BAD_PAGE
+    assert torch.isnan(out[0, :, 192:]).all()
+    assert torch.isfinite(out[0, :, :128]).all() and torch.isfinite(out[1]).all()
+
+
 def test_prefill_rejects_seq_len_different_from_q_len():
     prob = inputs.make("prefill", 2, 8, 2, 128, 64, [256, 256], seed=5)
     prob.seq_lens[1] = 255
