@@ -14,8 +14,11 @@
 // online-softmax state (the page fold of the CFR-Atlas README, "Core contract").
 //
 // Warp roles (128 + NT*128 threads, one CTA per SM):
-//   warp 0    TMA producer: the Q tiles once, then K and V blocks gathered page
-//             by page through the page table into a KV_STAGES-deep ring.
+//   warp 0    TMA producer: the Q tiles once, then K blocks gathered page by page
+//             through the page table into a KV_STAGES-deep ring.
+//   warp 3    TMA producer of the V ring (the same pages).  With one producer for
+//             both rings, its per-block work (page lookups, up to 32 box copies
+//             for 8-token pages) was the longest step of the suffix's pipeline.
 //   warp 1    allocates TMEM; one lane issues the MMAs:
 //               S  = Q K^T  (M=128, N=128, K=D; A and B from smem)  -> TMEM
 //               O += P V    (M=128, N=D, K=128; A = P from TMEM, B = V from smem)
@@ -27,7 +30,8 @@
 //             when the row max grew by more than 2^8 (exact: acc and l always
 //             share the reference max); write P as bf16 over its own S columns
 //             (plus the bf16 remainder P - bf16(P) for tiles whose rows see few
-//             keys, so that PV keeps ~16 bits of P there).  Epilogue: O / l.
+//             keys, so that PV keeps ~16 bits of P there).  Epilogue: O / l,
+//             written row by row through shared memory.
 // Every mbarrier wait is bounded; a CTA that gives up records ATLAS_DEV_TIMEOUT,
 // lets its copies and MMAs finish, frees TMEM and writes NaN.
 #include "internal.h"
