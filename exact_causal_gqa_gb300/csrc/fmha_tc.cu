@@ -529,41 +529,30 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 }
             }
             // Pass 1: row max of the raw scores (scale_log2 >= 0, so the scaled
-            // maximum is the maximum scaled), four chains of 3-input max.
+            // maximum is the maximum scaled), one per quarter, then combined.
             // Outer loops stay rolled: a fully unrolled body overflows the
             // instruction cache shared with the producer and MMA warps.
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            auto max32 = [&](const uint32_t (&v)[32]) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[e]),
-                                             __uint_as_float(v[e + 1]));
-            };
             if (all_visible) {
-                // Two 32-column buffers: the next quarter loads while this one is
-                // reduced (the waits name the loaded registers, so no use moves above).
-                uint32_t ma[32], mb[32];
-                tmem_ld32(ts, ma);
-                tmem_wait_ld32(ma);
-                tmem_ld32(ts + 32, mb);
-                max32(ma);
-                tmem_wait_ld32(mb);
-                tmem_ld32(ts + 64, ma);
-                max32(mb);
-                tmem_wait_ld32(ma);
-                tmem_ld32(ts + 96, mb);
-                max32(ma);
-                tmem_wait_ld32(mb);
-                max32(mb);
+                // The loads reduce as they read (tcgen05.ld.red): each returns its 32
+                // columns' maximum (the wait names the loaded registers, which the load
+                // writes until then).  Two loads in flight at a time measured slower.
+                uint32_t ma[32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    tmem_ld32_max(ts + cc * 32, ma, m4[cc]);
+                    tmem_wait_ld32_max(ma, m4[cc]);
+                }
             } else {
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     if ((q_none >> cc) & 1) continue;
                     uint32_t sr[32];
-                    tmem_ld32(ts + cc * 32, sr);
-                    tmem_wait_ld32(sr);
+                    float qm;
+                    tmem_ld32_max(ts + cc * 32, sr, qm);
+                    tmem_wait_ld32_max(sr, qm);
                     if ((q_full >> cc) & 1) {
-                        max32(sr);
+                        m4[0] = fmaxf(m4[0], qm);
                         continue;
                     }
 #pragma unroll

@@ -636,10 +636,14 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
             const uint32_t ts = tl + C::SC;
             const int nvis = lim_row - (kv_begin + j * BN);  // visible columns: [nlo, nvis)
             const int nlo = lo_row - (kv_begin + j * BN);
+            // The loads also return each half's maximum (tcgen05.ld.red), used when
+            // every column is visible.
             uint32_t sa[32], sb2[32];
-            tmem_ld32(ts, sa);
-            tmem_ld32(ts + 32, sb2);
-            tmem_wait_ld();
+            float qa, qb;
+            tmem_ld32_max(ts, sa, qa);
+            tmem_ld32_max(ts + 32, sb2, qb);
+            tmem_wait_ld32_max(sa, qa);
+            tmem_wait_ld32_max(sb2, qb);
             // raw scores; columns outside [nlo, nvis) are masked (they may hold
             // anything, NaN included: keys past the end or below the window)
             float sr[BN];
@@ -653,9 +657,8 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
             const bool all_visible = __all_sync(0xffffffffu, !valid || (nvis >= BN && nlo <= 0));
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (all_visible) {
-#pragma unroll
-                for (int e = 0; e < BN; e += 2)
-                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], sr[e], sr[e + 1]);
+                m4[0] = qa;
+                m4[1] = qb;
             } else {
 #pragma unroll
                 for (int e = 0; e < BN; e += 2) {
