@@ -162,7 +162,7 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=None,
             status=None, stream=None, split_tokens=0, debug_flags=0, events=None,
             window=0, softcap=0.0, sinks=None, q_lens=None, chunk_range=None,
-            phase=PHASE_ALL) -> _Launch:
+            phase=PHASE_ALL, sm_count=0) -> _Launch:
     L = _Launch()
     L.batch, L.q_len = q.shape[0], q.shape[2]
     L.max_pages_per_seq = page_table.shape[1]
@@ -185,6 +185,7 @@ def _launch(q, k_pages, page_table, out_dtype, out=None, lse=None, workspace=Non
     L.q_lens = _ptr(q_lens)
     L.chunk_range = _ptr(chunk_range)
     L.phase = phase
+    L.sm_count = sm_count
     return L
 
 
@@ -210,14 +211,15 @@ def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_
           head_dim, page_tokens, scale, *, out=None, out_dtype=None, lse=None,
           workspace=None, status=None, split_tokens=0, debug_flags=0, events=None,
           window=0, softcap=0.0, sinks=None, q_lens=None, chunk_range=None,
-          phase=PHASE_ALL):
+          phase=PHASE_ALL, sm_count=0):
     """``events``: optional ctypes array of three cudaEvent_t handles (see
     EventTimer) recorded around the main kernel and the merge.  ``window``,
     ``softcap`` and ``sinks`` (float32 CUDA tensor [n_q_heads]) select the score /
     mask variants; the defaults give plain causal attention.  ``q_lens`` (int32
     CUDA tensor [B]) makes the batch ragged: sequence b has q_lens[b] query rows.
     ``phase`` and ``chunk_range`` (int32 CUDA tensor [B][2]) spread one call over
-    several launches sharing ``workspace`` (atlas_launch.phase)."""
+    several launches sharing ``workspace`` (atlas_launch.phase).  ``sm_count`` > 0
+    plans for that many SMs instead of the device's (atlas_launch.sm_count)."""
     lib = load_library()
     for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
                     ("page_table", page_table), ("seq_lens", seq_lens)):
@@ -246,7 +248,7 @@ def _call(kind: str, q, k_pages, v_pages, page_table, seq_lens, n_q_heads, n_kv_
     L = _launch(q, k_pages, page_table, out_dtype, out, lse, None, status, stream,
                 split_tokens, debug_flags,
                 None if events is None else ctypes.cast(events, ctypes.c_void_p).value,
-                window, softcap, sinks, q_lens, chunk_range, phase)
+                window, softcap, sinks, q_lens, chunk_range, phase, sm_count)
     need = lib.atlas_attn_workspace_size(_KINDS[kind], n_q_heads, n_kv_heads, head_dim,
                                          page_tokens, ctypes.byref(L))
     if workspace is None and 0 < need < ctypes.c_size_t(-1).value:

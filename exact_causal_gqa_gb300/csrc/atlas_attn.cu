@@ -387,6 +387,7 @@ atlas_status run(atlas_kind kind, const void *q, const void *k_pages, const void
         tp.ws_acc = sp.ws_acc;
         tp.ws_ml = sp.ws_ml;
         tp.status = L->status_word;
+        tp.sms = L->sm_count > 0 ? L->sm_count : device_sm_count();
         if (ev[0] && cudaEventRecord(ev[0], stream) != cudaSuccess) return ATLAS_ERR_CUDA;
         err = f32 ? launch_fmha_tc_f32(tp, tmQ, tmK, tmV, stream)
                   : launch_fmha_tc(tp, tmQ, tmK, tmV, stream);

@@ -45,6 +45,7 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per block
+constexpr int kMaxItems = 64;  // work items of one CTA in persistent mode
 constexpr int kSlab = 128 * 128;  // one 64-element slab of a 128-row bf16 tile (128-byte rows)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows 256x
@@ -55,6 +56,17 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max
 // to 1.1e-2 above it, e.g. rows dominated by a few outlier keys).  The test runs in
 // the log domain against log2(w / (1 - w)) = log2(1/19).
 constexpr float kLog2HiLo = -4.2479275f;
+
+// One work item of a CTA: NT query tiles of one (sequence, kv head) over one key
+// range (all of it, or one split).
+struct TcWork {
+    int b, hkv, c, t0, tstep;  // tiles t0 + x * tstep, x < NT; split c
+    int qn, L, rows_unit;      // query rows of the sequence; shifted length; G * q_len
+    int kv_begin, kv_end, nb;  // key range and its 128-key blocks
+    bool hilo, tail_fix;       // hi + lo P on every block; last block partly past kv_end
+    int tail_first;            // first key row of the last block past kv_end
+    int state;                 // 0: compute; 1: nothing to compute; 2: bad seq_len
+};
 
 template <int NT, int D>
 struct Cfg {
@@ -87,13 +99,19 @@ struct Cfg {
     static constexpr int B_TAIL_READY = B_PVDONE + NT;  // single use
     static constexpr int B_TAIL = B_TAIL_READY + 1;     // single use
     static constexpr int B_FINAL = B_TAIL + 1;
-    static constexpr int kBars = B_FINAL + 1;
+    static constexpr int B_QEMPTY = B_FINAL + 1;  // an item's last S products done (Q free)
+    static constexpr int B_OFREE = B_QEMPTY + 1;  // [NT] an item's O read out (BM arrivals)
+    static constexpr int kBars = B_OFREE + NT;
     static constexpr int OFF_TMEM = OFF_BAR + kBars * 8;
     static constexpr int OFF_FLAG = OFF_TMEM + 8;
     // [NT][2] words of 4 bytes, one byte per warp of the tile: "this block needs P as
     // hi + lo", double-buffered by block parity
     static constexpr int OFF_VOTE = OFF_FLAG + 8;
-    static constexpr int kSmem = OFF_VOTE + NT * 8 + 1024;  // + slack to align the base
+    // the CTA's work items (persistent mode: up to kMaxItems), written once at the start
+    static constexpr int kItemSlots = NT == 2 ? kMaxItems : 1;
+    static constexpr int OFF_MASK = OFF_VOTE + 16;  // [2] words: items with a bad page id
+    static constexpr int OFF_ITEMS = OFF_MASK + 8;
+    static constexpr int kSmem = OFF_ITEMS + kItemSlots * (int)sizeof(TcWork) + 1024;  // + slack
     static_assert(kSmem <= 232448, "shared memory budget");
     // TMEM columns: NT=2 -> [S0 | O0 | S1 | O1]; NT=1 -> [S(buf 0) | S(buf 1) | O]
     __device__ static constexpr uint32_t s_col(int x, int b) {
@@ -141,7 +159,85 @@ __device__ void nan_row(const TcParams &p, int b, int hkv, int f) {
     if (p.lse) p.lse[row] = nan;
 }
 
-template <int NT, int D>
+template <int NT>
+__device__ TcWork tc_work(const TcParams &p, int u, int c, int t0, int tstep, int split_keys) {
+    TcWork w{};
+    w.b = u / p.Hkv;
+    w.hkv = u % p.Hkv;
+    w.c = c;
+    w.t0 = t0;
+    w.tstep = tstep;
+    const int seq_len = p.seq_lens[w.b];
+    w.qn = p.q_lens ? p.q_lens[w.b] : p.q_len;  // query rows of this sequence
+    w.rows_unit = p.G * p.q_len;
+    // Both tiles cover the same prompt rows, so their key ranges agree.
+    const int f0 = t0 * BM;
+    const int f_last = min(f0 + BM, w.rows_unit) - 1;
+    const bool spans = (f_last / p.q_len) != (f0 / p.q_len);
+    const int i_min = spans ? 0 : f0 % p.q_len;
+    if (w.qn < 0 || w.qn > p.q_len || seq_len < w.qn || seq_len > p.max_pages * p.P ||
+        (p.require_full && seq_len != w.qn)) {
+        w.state = 2;
+        return w;
+    }
+    if (i_min >= w.qn) {  // only padding rows of a ragged sequence
+        w.state = 1;
+        return w;
+    }
+    // Last real row of the tiles; with L shifted by q_len - qn, row i sits at
+    // position L - q_len + i = seq_len - qn + i as in a full batch.
+    const int i_max = min(spans ? p.q_len - 1 : f_last % p.q_len, w.qn - 1);
+    w.L = seq_len - w.qn + p.q_len;
+    const int kv_hi = w.L - p.q_len + i_max + 1;  // keys the tiles' last row sees
+    // Keys the tiles' first row sees (its window may cut that short).
+    const int kv_min = p.window > 0 ? min(w.L - p.q_len + i_min + 1, p.window)
+                                    : w.L - p.q_len + i_min + 1;
+    // Blocks below every row's window are skipped whole.
+    const int kv_lo = p.window > 0 ? max(0, w.L - p.q_len + i_min + 1 - p.window) / BN * BN : 0;
+    w.kv_begin = kv_lo;
+    w.kv_end = kv_hi;
+    if (p.split) {
+        w.kv_begin = max(c * split_keys, kv_lo);
+        w.kv_end = min(kv_hi, c * split_keys + split_keys);
+        if (w.kv_begin >= w.kv_end) {
+            w.state = 1;
+            return w;
+        }
+    }
+    w.nb = (w.kv_end - w.kv_begin + BN - 1) / BN;
+    w.hilo = kv_min < p.hilo_below;
+    const int last_kb = w.kv_begin + (w.nb - 1) * BN;
+    w.tail_fix = w.kv_end < last_kb + BN;
+    w.tail_first = w.kv_end - last_kb;
+    return w;
+}
+
+// Direct mode: item r of the heavy-first order (the latest prompt rows first).
+template <int NT>
+__device__ void tc_direct_item(const TcParams &p, int r, int &u, int &t0, int &tstep) {
+    const int units = p.B * p.Hkv;
+    if (p.tiles_per_head > 0) {
+        const int heads = p.G / NT;  // head groups of NT heads
+        const int per = units * heads;
+        const int rest = r % per;
+        u = rest / heads;
+        const int qi = p.tiles_per_head - 1 - r / per;
+        t0 = (rest % heads) * NT * p.tiles_per_head + qi;
+        tstep = p.tiles_per_head;
+    } else {
+        u = r % units;
+        t0 = r / units;
+        tstep = 0;
+    }
+}
+
+// Persistent mode: the i-th item of CTA k of `ctas`, snake order over the
+// heavy-first list (a heavy item pairs with a light one in the next pass).
+__device__ __forceinline__ int tc_persist_item(int k, int i, int ctas) {
+    return i * ctas + ((i & 1) ? ctas - 1 - k : k);
+}
+
+template <int NT, int D, bool PERSIST>
 __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const TcParams p) {
@@ -158,110 +254,110 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #define BAR(i) (sb + C::OFF_BAR + 8u * (uint32_t)(i))
 
-    // ------------------------------------------------------------ work item
-    const int units = p.B * p.Hkv;
-    int u, c, t0, tstep;  // tiles t0 + x * tstep, x < NT
-    int split_keys = p.chunk;  // keys per split (split mode)
-    if (p.split && p.balanced) {
-        // longest-first work item (the V ring is free until the producer starts)
-        const TcItem it = tc_balanced_item(p, blockIdx.x + blockIdx.y * gridDim.x,
-                                           reinterpret_cast<int *>(smem + C::OFF_V));
-        if (it.b < 0) return;
-        c = it.split;
-        u = it.b * p.Hkv + it.hkv;
-        t0 = it.tile;
-        tstep = 0;
-        split_keys = it.split_keys;
-    } else if (p.split) {
-        c = blockIdx.x;
-        u = blockIdx.y / p.tiles_per_unit;
-        t0 = blockIdx.y % p.tiles_per_unit;
-        tstep = 0;
+    // ------------------------------------------------------------ work items
+    // One item in the grid-per-item modes.  Persistent mode (direct prefill, two
+    // tiles per CTA): this CTA's items in a snake order over the heavy-first list;
+    // every role walks them, and the barrier phases run on across items (counted in
+    // blocks and items), so the next item's Q, K/V and first S products overlap the
+    // current item's last blocks and epilogue.
+    constexpr bool persist = PERSIST;
+    int n_items = 1;
+    TcWork w0{};
+    if (PERSIST) {
+        const int total = p.B * p.Hkv * (p.G / NT) * p.tiles_per_head;
+        n_items = 0;
+        while (n_items < kMaxItems && tc_persist_item(blockIdx.x, n_items, gridDim.x) < total)
+            ++n_items;
     } else {
-        c = 0;
-        const int r = blockIdx.x;
-        if (p.tiles_per_head > 0) {  // heavy tiles (late prompt rows) first
-            const int heads = p.G / NT;  // head groups of NT heads
-            const int per = units * heads;
-            const int rest = r % per;
-            u = rest / heads;
-            const int qi = p.tiles_per_head - 1 - r / per;
-            t0 = (rest % heads) * NT * p.tiles_per_head + qi;
-            tstep = p.tiles_per_head;
-        } else {
-            u = r % units;
-            t0 = r / units;
+        int u, c, t0, tstep;
+        int split_keys = p.chunk;  // keys per split (split mode)
+        if (p.split && p.balanced) {
+            // longest-first work item (the V ring is free until the producer starts)
+            const TcItem it = tc_balanced_item(p, blockIdx.x + blockIdx.y * gridDim.x,
+                                               reinterpret_cast<int *>(smem + C::OFF_V));
+            if (it.b < 0) return;
+            c = it.split;
+            u = it.b * p.Hkv + it.hkv;
+            t0 = it.tile;
             tstep = 0;
+            split_keys = it.split_keys;
+        } else if (p.split) {
+            c = blockIdx.x;
+            u = blockIdx.y / p.tiles_per_unit;
+            t0 = blockIdx.y % p.tiles_per_unit;
+            tstep = 0;
+        } else {
+            c = 0;
+            tc_direct_item<NT>(p, blockIdx.x, u, t0, tstep);
         }
+        // A pass of a call spread over several launches computes some splits only.
+        const int b = u / p.Hkv;
+        if (p.split && p.chunk_range &&
+            (c < p.chunk_range[2 * b] || c >= p.chunk_range[2 * b + 1]))
+            return;
+        w0 = tc_work<NT>(p, u, c, t0, tstep, split_keys);
     }
-    const int b = u / p.Hkv, hkv = u % p.Hkv;
-    // A pass of a call spread over several launches computes some splits only.
-    if (p.split && p.chunk_range && (c < p.chunk_range[2 * b] || c >= p.chunk_range[2 * b + 1]))
-        return;
-    const int seq_len = p.seq_lens[b];
-    const int qn = p.q_lens ? p.q_lens[b] : p.q_len;  // query rows of this sequence
-    const int rows_unit = p.G * p.q_len;
-    // Both tiles cover the same prompt rows, so their key ranges agree.
-    const int f0 = t0 * BM;
-    const int f_last = min(f0 + BM, rows_unit) - 1;
-    const bool spans = (f_last / p.q_len) != (f0 / p.q_len);
-    const int i_min = spans ? 0 : f0 % p.q_len;
-
-    if (qn < 0 || qn > p.q_len || seq_len < qn || seq_len > p.max_pages * p.P ||
-        (p.require_full && seq_len != qn)) {
-        if (threadIdx.x == 0 && c == 0 && p.status) atomicOr(p.status, ATLAS_DEV_BAD_SEQLEN);
-        const int rows_valid = (qn >= 0 && qn <= p.q_len) ? qn : p.q_len;
-        if (!p.split && threadIdx.x < NT * BM) {
-            const int f = (t0 + (int)(threadIdx.x / BM) * tstep) * BM + threadIdx.x % BM;
-            if (f < rows_unit && f % p.q_len < rows_valid) nan_row<D>(p, b, hkv, f);
+    TcWork *const items = reinterpret_cast<TcWork *>(smem + C::OFF_ITEMS);
+    // Items not computed (bit set): a bad seq_len or a page id outside the pool (rows
+    // NaN), or nothing to compute.  The page ids of every item's key range are
+    // checked by the whole CTA at once; the result is the same in every thread.
+    uint32_t *bad_words = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
+    if (threadIdx.x == 0) bad_words[0] = bad_words[1] = 0u;
+    __syncthreads();
+    uint64_t skip = 0, bad = 0;
+    for (int it = 0; it < n_items; ++it) {
+        TcWork w = w0;
+        if (PERSIST) {
+            int u, t0, tstep;
+            tc_direct_item<NT>(p, tc_persist_item(blockIdx.x, it, gridDim.x), u, t0, tstep);
+            w = tc_work<NT>(p, u, 0, t0, tstep, p.chunk);
+            if (threadIdx.x == 0) items[it] = w;  // read by every role after the barriers
         }
-        return;  // split mode: the merge writes NaN rows for this sequence
-    }
-    if (i_min >= qn) return;  // only padding rows of a ragged sequence
-    // Last real row of the tiles; with L shifted by q_len - qn, row i sits at
-    // position L - q_len + i = seq_len - qn + i as in a full batch.
-    const int i_max = min(spans ? p.q_len - 1 : f_last % p.q_len, qn - 1);
-    const int L = seq_len - qn + p.q_len;
-    const int kv_hi = L - p.q_len + i_max + 1;   // keys the tiles' last row sees
-    // Keys the tiles' first row sees (its window may cut that short).
-    const int kv_min = p.window > 0 ? min(L - p.q_len + i_min + 1, p.window)
-                                    : L - p.q_len + i_min + 1;
-    // Blocks below every row's window are skipped whole.
-    const int kv_lo = p.window > 0 ? max(0, L - p.q_len + i_min + 1 - p.window) / BN * BN : 0;
-    int kv_begin = kv_lo, kv_end = kv_hi;
-    if (p.split) {
-        kv_begin = max(c * split_keys, kv_lo);
-        kv_end = min(kv_hi, c * split_keys + split_keys);
-        if (kv_begin >= kv_end) return;
-    }
-    const int nb = (kv_end - kv_begin + BN - 1) / BN;
-    {
-        const int pg0 = kv_begin / p.P, pg1 = (kv_end - 1) / p.P;
-        bool bad = false;
+        if (w.state != 0) {
+            skip |= 1ull << it;
+            continue;
+        }
+        const int pg0 = w.kv_begin / p.P, pg1 = (w.kv_end - 1) / p.P;
         for (int pg = pg0 + (int)threadIdx.x; pg <= pg1; pg += blockDim.x) {
-            const int id = p.page_table[(int64_t)b * p.max_pages + pg];
-            bad |= (id < 0 || id >= p.num_pages);
+            const int id = p.page_table[(int64_t)w.b * p.max_pages + pg];
+            if (id < 0 || id >= p.num_pages) bad |= 1ull << it;
         }
-        if (__syncthreads_or(bad)) {
+    }
+    if (bad) {
+        atomicOr(bad_words, (uint32_t)bad);
+        atomicOr(bad_words + 1, (uint32_t)(bad >> 32));
+    }
+    __syncthreads();
+    const uint64_t bad_page = bad_words[0] | ((uint64_t)bad_words[1] << 32);
+    skip |= bad_page;
+    for (int it = 0; skip && it < n_items; ++it) {
+        if (!((skip >> it) & 1)) continue;
+        const TcWork &w = PERSIST ? items[it] : w0;
+        if (w.state == 2) {
+            if (threadIdx.x == 0 && w.c == 0 && p.status) atomicOr(p.status, ATLAS_DEV_BAD_SEQLEN);
+            const int rows_valid = (w.qn >= 0 && w.qn <= p.q_len) ? w.qn : p.q_len;
+            if (!p.split && threadIdx.x < NT * BM) {
+                const int f = (w.t0 + (int)(threadIdx.x / BM) * w.tstep) * BM + threadIdx.x % BM;
+                if (f < w.rows_unit && f % p.q_len < rows_valid) nan_row<D>(p, w.b, w.hkv, f);
+            }
+            // split mode: the merge writes NaN rows for this sequence
+        } else if ((bad_page >> it) & 1) {
             if (threadIdx.x == 0 && p.status) atomicOr(p.status, ATLAS_DEV_BAD_PAGE);
             if (threadIdx.x < NT * BM) {
-                const int f = (t0 + (int)(threadIdx.x / BM) * tstep) * BM + threadIdx.x % BM;
-                if (f < rows_unit && f % p.q_len < qn) {
+                const int f = (w.t0 + (int)(threadIdx.x / BM) * w.tstep) * BM + threadIdx.x % BM;
+                if (f < w.rows_unit && f % p.q_len < w.qn) {
                     if (!p.split) {
-                        nan_row<D>(p, b, hkv, f);
+                        nan_row<D>(p, w.b, w.hkv, f);
                     } else {
-                        float *ml = p.ws_ml + (tile_row(p, b, hkv, f) * p.n_chunks + c) * 2;
+                        float *ml =
+                            p.ws_ml + (tile_row(p, w.b, w.hkv, f) * p.n_chunks + w.c) * 2;
                         ml[0] = ml[1] = __int_as_float(0x7fc00000);
                     }
                 }
             }
-            return;
         }
     }
-    const bool hilo = kv_min < p.hilo_below;
-    const int last_kb = kv_begin + (nb - 1) * BN;
-    const bool tail_fix = kv_end < last_kb + BN;
-    const int tail_first = kv_end - last_kb;
+    if (skip == (n_items == 64 ? ~0ull : (1ull << n_items) - 1)) return;
 
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
@@ -280,6 +376,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         mbar_init(BAR(C::B_TAIL_READY), 1);
         mbar_init(BAR(C::B_TAIL), 1);
         mbar_init(BAR(C::B_FINAL), 1);
+        mbar_init(BAR(C::B_QEMPTY), 1);
+        for (int x = 0; x < NT; ++x) mbar_init(BAR(C::B_OFREE + x), BM);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -298,54 +396,71 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         // kb / P + bx from its first row, and a block's pages lie in one 32-page line
         // of the cache: lane bx looks its page up with one shuffle and issues box bx.
         const int kv = warp == 0 ? 0 : 1;
-        if (kv == 0 && lane == 0) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            mbar_arrive_expect_tx(BAR(C::B_Q), NT * kTileBytes);
-            for (int x = 0; x < NT; ++x) {
-                const int qrow = (int)tile_row(p, b, hkv, (t0 + x * tstep) * BM);
-#pragma unroll
-                for (int sl = 0; sl < C::kSlabs; ++sl)
-                    tma_load_2d(sb + C::OFF_Q + x * kTileBytes + sl * kSlab, &tmQ, 64 * sl, qrow,
-                                BAR(C::B_Q));
-            }
+        if (lane == 0) {
+            prefetch_tmap(kv == 0 ? &tmK : &tmV);
+            if (kv == 0) prefetch_tmap(&tmQ);
         }
-        if (kv == 1 && lane == 0) prefetch_tmap(&tmV);
         const CUtensorMap *map = kv == 0 ? &tmK : &tmV;
         const uint32_t ring = sb + (kv == 0 ? C::OFF_K : C::OFF_V);
         const int bar_full = kv == 0 ? C::B_KFULL : C::B_VFULL;
         const int bar_empty = kv == 0 ? C::B_KEMPTY : C::B_VEMPTY;
         const int lp = 31 - __clz(p.P);  // log2(P)
-        PageIdCache pages{p.page_table + (int64_t)b * p.max_pages, (kv_end - 1) >> lp};
-        int issued = 0;
-        for (int j = 0; j < nb; ++j) {
-            const int s = j % S, use = j / S;
-            const int kb = kv_begin + j * BN;
-            const int nbox = (min(BN, kv_end - kb) + p.P - 1) >> lp;  // <= 16
-            const int y = (pages.get_line(kb >> lp, lane < nbox ? lane : 0) * p.Hkv + hkv) << lp;
-            if (use > 0 && !wait_warp(BAR(bar_empty + s), (use - 1) & 1, abort_flag)) {
-                failed = true;
-                break;
-            }
-            if (lane < nbox) {
-                if (lane == 0)
-                    mbar_arrive_expect_tx(BAR(bar_full + s),
-                                          (uint32_t)(nbox << lp) * 128u * C::kSlabs);
-                __syncwarp((1u << nbox) - 1u);
+        int g = 0;   // blocks of this ring issued so far (all items)
+        int nq = 0;  // Q tile pairs loaded so far
+        for (int it = 0; it < n_items && !failed; ++it) {
+            if ((skip >> it) & 1) continue;
+            const TcWork &w = PERSIST ? items[it] : w0;
+            if (kv == 0) {
+                // The previous item's Q tiles are free once its last S products are done.
+                if (nq > 0 && !wait_warp(BAR(C::B_QEMPTY), (nq - 1) & 1, abort_flag)) {
+                    failed = true;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(BAR(C::B_Q), NT * kTileBytes);
+                    for (int x = 0; x < NT; ++x) {
+                        const int qrow = (int)tile_row(p, w.b, w.hkv, (w.t0 + x * w.tstep) * BM);
 #pragma unroll
-                for (int sl = 0; sl < C::kSlabs; ++sl)
-                    tma_load_2d(ring + s * kTileBytes + sl * kSlab + (lane << lp) * 128, map,
-                                64 * sl, y, BAR(bar_full + s));
+                        for (int sl = 0; sl < C::kSlabs; ++sl)
+                            tma_load_2d(sb + C::OFF_Q + x * kTileBytes + sl * kSlab, &tmQ,
+                                        64 * sl, qrow, BAR(C::B_Q));
+                    }
+                }
+                ++nq;
             }
-            __syncwarp();
-            issued = j + 1;
+            PageIdCache pages{p.page_table + (int64_t)w.b * p.max_pages, (w.kv_end - 1) >> lp};
+            for (int j = 0; j < w.nb; ++j) {
+                const int s = g % S, use = g / S;
+                const int kb = w.kv_begin + j * BN;
+                const int nbox = (min(BN, w.kv_end - kb) + p.P - 1) >> lp;  // <= 16
+                const int y =
+                    (pages.get_line(kb >> lp, lane < nbox ? lane : 0) * p.Hkv + w.hkv) << lp;
+                if (use > 0 && !wait_warp(BAR(bar_empty + s), (use - 1) & 1, abort_flag)) {
+                    failed = true;
+                    break;
+                }
+                if (lane < nbox) {
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(BAR(bar_full + s),
+                                              (uint32_t)(nbox << lp) * 128u * C::kSlabs);
+                    __syncwarp((1u << nbox) - 1u);
+#pragma unroll
+                    for (int sl = 0; sl < C::kSlabs; ++sl)
+                        tma_load_2d(ring + s * kTileBytes + sl * kSlab + (lane << lp) * 128, map,
+                                    64 * sl, y, BAR(bar_full + s));
+                }
+                __syncwarp();
+                ++g;
+            }
         }
         if (failed && lane == 0) {
             *abort_flag = 1;
             int no_abort = 0;
-            if (kv == 0) mbar_wait_bounded(BAR(C::B_Q), 0, &no_abort, kWaitLimitNs);
-            for (int j = max(0, issued - S); j < issued; ++j)
-                mbar_wait_bounded(BAR(bar_full + j % S), (j / S) & 1, &no_abort, kWaitLimitNs);
+            // Let the copies in flight land before the CTA's shared memory goes away.
+            if (kv == 0 && nq > 0)
+                mbar_wait_bounded(BAR(C::B_Q), (nq - 1) & 1, &no_abort, kWaitLimitNs);
+            for (int k = max(0, g - S); k < g; ++k)
+                mbar_wait_bounded(BAR(bar_full + k % S), (k / S) & 1, &no_abort, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -353,104 +468,132 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(128, 128, false, p.negate_scores != 0);
             constexpr uint32_t idPV = idesc_bf16_f32(128, D, true);
-            bool ok = mbar_wait_bounded(BAR(C::B_Q), 0, abort_flag, kWaitLimitNs);
-            tc_fence_after();
-            // S_x(j) = Q_x K_j^T into S buffer j % SB of tile x.  Tile 0 waits for
-            // K_j; the last tile releases its stage.
-            auto issue_s = [&](int j, int x) -> bool {
-                const int s = j % S;
-                if (x == 0) {
-                    if (!mbar_wait_bounded(BAR(C::B_KFULL + s), (j / S) & 1, abort_flag,
-                                           kWaitLimitNs))
-                        return false;
-                    tc_fence_after();
-                }
-                // Descriptors built once per operand base; the K slices step through
-                // the 14-bit address field (16-byte units), which no smem offset here
-                // can carry out of.
-                const uint64_t kd = sdesc_sw128(sb + C::OFF_K + s * kTileBytes, 16, 1024);
-                const uint64_t qd = sdesc_sw128(sb + C::OFF_Q + x * kTileBytes, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
-                    umma_bf16(tmem + C::s_col(x, j % SB), qd + off, kd + off, idS, kk > 0);
-                }
-                umma_commit(BAR(C::B_SFULL + x * SB + j % SB));
-                if (x == NT - 1) {
-                    umma_commit(BAR(C::B_KEMPTY + s));
-                }
-                return true;
-            };
-            for (int j = 0; ok && j < min(SB, nb); ++j)
-#pragma unroll
-                for (int x = 0; x < NT; ++x)
-                    if (ok) ok = issue_s(j, x);
-            for (int j = 0; ok && j < nb; ++j) {
-                const int s = j % S;
-#pragma unroll
-                for (int x = 0; x < NT; ++x) {
-                    if (!mbar_wait_bounded(BAR(C::B_PFULL + x), j & 1, abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
+            bool ok = true;
+            int g = 0;      // blocks of earlier items
+            int nq = 0;     // items so far
+            int ntail = 0;  // tail fix-ups so far
+            for (int it = 0; ok && it < n_items; ++it) {
+                if ((skip >> it) & 1) continue;
+                const TcWork &w = PERSIST ? items[it] : w0;
+                const int nb = w.nb;
+                ok = mbar_wait_bounded(BAR(C::B_Q), nq & 1, abort_flag, kWaitLimitNs);
+                tc_fence_after();
+                if (!ok) break;
+                // S_x(j) = Q_x K_j^T into S buffer (g + j) % SB of tile x.  Tile 0 waits
+                // for K_j; the last tile releases its stage, and after the item's last
+                // block also the Q tiles.
+                auto issue_s = [&](int j, int x) -> bool {
+                    const int G = g + j, s = G % S;
                     if (x == 0) {
-                        if (!mbar_wait_bounded(BAR(C::B_VFULL + s), (j / S) & 1, abort_flag,
+                        if (!mbar_wait_bounded(BAR(C::B_KFULL + s), (G / S) & 1, abort_flag,
+                                               kWaitLimitNs))
+                            return false;
+                        tc_fence_after();
+                    }
+                    // Descriptors built once per operand base; the K slices step through
+                    // the 14-bit address field (16-byte units), which no smem offset here
+                    // can carry out of.
+                    const uint64_t kd = sdesc_sw128(sb + C::OFF_K + s * kTileBytes, 16, 1024);
+                    const uint64_t qd = sdesc_sw128(sb + C::OFF_Q + x * kTileBytes, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
+                        umma_bf16(tmem + C::s_col(x, G % SB), qd + off, kd + off, idS, kk > 0);
+                    }
+                    umma_commit(BAR(C::B_SFULL + x * SB + G % SB));
+                    if (x == NT - 1) {
+                        umma_commit(BAR(C::B_KEMPTY + s));
+                        if (j == nb - 1) umma_commit(BAR(C::B_QEMPTY));
+                    }
+                    return true;
+                };
+                for (int j = 0; ok && j < min(SB, nb); ++j)
+#pragma unroll
+                    for (int x = 0; x < NT; ++x)
+                        if (ok) ok = issue_s(j, x);
+                for (int j = 0; ok && j < nb; ++j) {
+                    const int G = g + j, s = G % S;
+#pragma unroll
+                    for (int x = 0; x < NT; ++x) {
+                        if (!mbar_wait_bounded(BAR(C::B_PFULL + x), G & 1, abort_flag,
                                                kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
-                        if (j == nb - 1 && tail_fix) {
-                            // Hand the landed last V block to the fix-up warp (only this
-                            // thread observes every phase of the V ring in order).
-                            mbar_arrive(BAR(C::B_TAIL_READY));
-                            if (!mbar_wait_bounded(BAR(C::B_TAIL), 0, abort_flag, kWaitLimitNs)) {
+                        if (x == 0) {
+                            if (!mbar_wait_bounded(BAR(C::B_VFULL + s), (G / S) & 1, abort_flag,
+                                                   kWaitLimitNs)) {
                                 ok = false;
                                 break;
                             }
+                            if (j == nb - 1 && w.tail_fix) {
+                                // Hand the landed last V block to the fix-up warp (only
+                                // this thread observes every phase of the V ring in order).
+                                mbar_arrive(BAR(C::B_TAIL_READY));
+                                if (!mbar_wait_bounded(BAR(C::B_TAIL), ntail & 1, abort_flag,
+                                                       kWaitLimitNs)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ++ntail;
+                            }
                         }
-                    }
-                    tc_fence_after();
-                    const uint64_t vd = sdesc_sw128(sb + C::OFF_V + s * kTileBytes, kSlab, 1024);
-                    const uint32_t pcol = tmem + C::s_col(x, j % SB);
-                    // keys 16kk .. 16kk+15 of P sit in columns 32*(kk/2) + 8*(kk%2) .. +8,
-                    // their remainders 16 columns further on.  V slice kk starts 2048
-                    // bytes (128 descriptor units) after slice kk-1.
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16_tmem_a(tmem + C::o_col(x), pcol + (kk >> 1) * 32 + (kk & 1) * 8,
-                                         vd + kk * 128u, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    // The softmax's vote for this block (one byte per warp, written before
-                    // its P arrival), read once the hi products are queued so its latency
-                    // hides there.  The lo product leaves the rows of warps that did not
-                    // ask for it unchanged: their lo columns hold no P.
-                    const uint32_t vote = *reinterpret_cast<volatile uint32_t *>(
-                        smem + C::OFF_VOTE + (x * 2 + (j & 1)) * 4);
-                    if (hilo || vote != 0u) {
-                        uint32_t off_lanes[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            off_lanes[q] = (hilo || ((vote >> (8 * q)) & 0xffu)) ? 0u : 0xffffffffu;
+                        // The item's first PV overwrites O: the previous item's
+                        // epilogue must have read it out.
+                        if (j == 0 && nq > 0 &&
+                            !mbar_wait_bounded(BAR(C::B_OFREE + x), (nq - 1) & 1, abort_flag,
+                                               kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t vd =
+                            sdesc_sw128(sb + C::OFF_V + s * kTileBytes, kSlab, 1024);
+                        const uint32_t pcol = tmem + C::s_col(x, G % SB);
+                        // keys 16kk .. 16kk+15 of P sit in columns 32*(kk/2) + 8*(kk%2) ..
+                        // +8, their remainders 16 columns further on.  V slice kk starts
+                        // 2048 bytes (128 descriptor units) after slice kk-1.
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_bf16_tmem_a_masked(tmem + C::o_col(x),
-                                                    pcol + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
-                                                    vd + kk * 128u, idPV, off_lanes);
-                    }
-                    umma_commit(BAR(C::B_PVDONE + x));
-                    // The V stage is free once the last tile's PV has read it: release
-                    // it before S_x(j + SB) waits for its K block.
-                    if (x == NT - 1) umma_commit(BAR(C::B_VEMPTY + s));
-                    // Ping-pong: S_x(j + SB) follows PV_x(j) at once, so tile x starts
-                    // its next softmax while the other tile's P is still being made.
-                    // It writes the S buffer that PV_x(j) reads P_x(j) from; the
-                    // tcgen05.mma operations of one thread run in issue order, so
-                    // PV_x(j) has read its operand before S_x(j + SB) writes there.
-                    if (j + SB < nb && !issue_s(j + SB, x)) {
-                        ok = false;
-                        break;
+                            umma_bf16_tmem_a(tmem + C::o_col(x),
+                                             pcol + (kk >> 1) * 32 + (kk & 1) * 8,
+                                             vd + kk * 128u, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        // The softmax's vote for this block (one byte per warp, written
+                        // before its P arrival), read once the hi products are queued so
+                        // its latency hides there.  The lo product leaves the rows of
+                        // warps that did not ask for it unchanged: their lo columns hold
+                        // no P.
+                        const uint32_t vote = *reinterpret_cast<volatile uint32_t *>(
+                            smem + C::OFF_VOTE + (x * 2 + (G & 1)) * 4);
+                        if (w.hilo || vote != 0u) {
+                            uint32_t off_lanes[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                off_lanes[q] =
+                                    (w.hilo || ((vote >> (8 * q)) & 0xffu)) ? 0u : 0xffffffffu;
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                umma_bf16_tmem_a_masked(tmem + C::o_col(x),
+                                                        pcol + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+                                                        vd + kk * 128u, idPV, off_lanes);
+                        }
+                        umma_commit(BAR(C::B_PVDONE + x));
+                        // The V stage is free once the last tile's PV has read it: release
+                        // it before S_x(j + SB) waits for its K block.
+                        if (x == NT - 1) umma_commit(BAR(C::B_VEMPTY + s));
+                        // Ping-pong: S_x(j + SB) follows PV_x(j) at once, so tile x starts
+                        // its next softmax while the other tile's P is still being made.
+                        // It writes the S buffer that PV_x(j) reads P_x(j) from; the
+                        // tcgen05.mma operations of one thread run in issue order, so
+                        // PV_x(j) has read its operand before S_x(j + SB) writes there.
+                        if (j + SB < nb && !issue_s(j + SB, x)) {
+                            ok = false;
+                            break;
+                        }
                     }
                 }
-                if (!ok) break;
+                g += nb;
+                ++nq;
             }
             if (!ok) {
                 failed = true;
@@ -464,22 +607,29 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         __syncwarp();
     } else if (warp == 2) {
         // -------------------------------------------------------- tail fix-up
-        if (tail_fix) {
-            const int s = (nb - 1) % S;
-            if (wait_warp(BAR(C::B_TAIL_READY), 0, abort_flag)) {
-                const uint32_t vbase = sb + C::OFF_V + s * kTileBytes;
-                constexpr int kChunks = 8 * C::kSlabs;  // 16-byte chunks per V row
-                for (int idx = lane; idx < (BN - tail_first) * kChunks; idx += 32) {
-                    const int row = tail_first + idx / kChunks, q = idx % kChunks;
-                    st_shared_v4(vbase + (q / 8) * kSlab + row * 128 + (q % 8) * 16, 0u, 0u, 0u,
-                                 0u);
+        int g = 0, ntail = 0;
+        for (int it = 0; it < n_items && !failed; ++it) {
+            if ((skip >> it) & 1) continue;
+            const TcWork &w = PERSIST ? items[it] : w0;
+            if (w.tail_fix) {
+                const int s = (g + w.nb - 1) % S;
+                if (wait_warp(BAR(C::B_TAIL_READY), ntail & 1, abort_flag)) {
+                    const uint32_t vbase = sb + C::OFF_V + s * kTileBytes;
+                    constexpr int kChunks = 8 * C::kSlabs;  // 16-byte chunks per V row
+                    for (int idx = lane; idx < (BN - w.tail_first) * kChunks; idx += 32) {
+                        const int row = w.tail_first + idx / kChunks, q = idx % kChunks;
+                        st_shared_v4(vbase + (q / 8) * kSlab + row * 128 + (q % 8) * 16, 0u, 0u,
+                                     0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(C::B_TAIL));
+                    ++ntail;
+                } else {
+                    failed = true;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(C::B_TAIL));
-            } else {
-                failed = true;
             }
+            g += w.nb;
         }
     } else if (warp >= C::kSoftmaxWarp0) {
         // -------------------------------------------------------- softmax
@@ -487,20 +637,29 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         const int x = (warp - C::kSoftmaxWarp0) / 4;  // tile of this warpgroup
         const int q4 = warp % 4;                      // TMEM lane quadrant
         const int r = q4 * 32 + lane;
-        const int f = (t0 + x * tstep) * BM + r;
-        const bool valid = f < rows_unit && f % p.q_len < qn;  // padding rows are not queries
-        const int i = valid ? f % p.q_len : 0;
-        const int lim_row = valid ? min(L - p.q_len + i + 1, kv_end) : 0;
-        const int lo_row = (valid && p.window > 0) ? max(0, L - p.q_len + i + 1 - p.window) : 0;
         const bool capped = p.softcap_log2 > 0.f;
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
         const uint32_t to = tl + C::o_col(x);
+        bool ok = true;
+        int g = 0;  // blocks of earlier items
+        int it = 0;
+        for (; ok && it < n_items; ++it) {
+        if ((skip >> it) & 1) continue;
+        const TcWork &w = PERSIST ? items[it] : w0;
+        const int b = w.b, hkv = w.hkv, c = w.c, kv_begin = w.kv_begin, nb = w.nb;
+        const bool hilo = w.hilo;
+        const int f = (w.t0 + x * w.tstep) * BM + r;
+        const bool valid = f < w.rows_unit && f % p.q_len < w.qn;  // padding rows: no queries
+        const int i = valid ? f % p.q_len : 0;
+        const int lim_row = valid ? min(w.L - p.q_len + i + 1, w.kv_end) : 0;
+        const int lo_row =
+            (valid && p.window > 0) ? max(0, w.L - p.q_len + i + 1 - p.window) : 0;
         float m_used = -INFINITY, l = 0.f;
         float log2_l = -INFINITY;  // log2(l), refreshed at the end of each block
-        bool ok = true;
         for (int j = 0; j < nb; ++j) {
-            const int bsel = j % SB;
-            if (!wait_warp(BAR(C::B_SFULL + x * SB + bsel), (j / SB) & 1, abort_flag)) {
+            const int G = g + j;  // block count over the CTA's items: barrier phases
+            const int bsel = G % SB;
+            if (!wait_warp(BAR(C::B_SFULL + x * SB + bsel), (G / SB) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -592,7 +751,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 const bool need = mx - mref > kLog2HiLo + log2_l + log2_corr;
                 split_blk = __any_sync(0xffffffffu, need);
                 if (lane == 0)
-                    smem[C::OFF_VOTE + (x * 2 + (j & 1)) * 4 + q4] = split_blk ? 1 : 0;
+                    smem[C::OFF_VOTE + (x * 2 + (G & 1)) * 4 + q4] = split_blk ? 1 : 0;
             }
 
             // Pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs, written over columns
@@ -707,7 +866,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             // PV(j-1) off the critical path.  With one S buffer S(j) was issued after
             // PV(j-1) by the same thread, and its commit tracks every earlier MMA, so
             // S being full already says so.
-            if (SB > 1 && j > 0 && !wait_warp(BAR(C::B_PVDONE + x), (j - 1) & 1, abort_flag)) {
+            if (SB > 1 && j > 0 && !wait_warp(BAR(C::B_PVDONE + x), (G - 1) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -727,7 +886,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             tc_fence_before();
             mbar_arrive(BAR(C::B_PFULL + x));
         }
-        if (ok && !wait_warp(BAR(C::B_PVDONE + x), (nb - 1) & 1, abort_flag)) ok = false;
+        if (ok && !wait_warp(BAR(C::B_PVDONE + x), (g + nb - 1) & 1, abort_flag)) ok = false;
         if (!ok) {
             failed = true;
             *abort_flag = 1;
@@ -765,6 +924,35 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 uint32_t o[32];
                 tmem_ld32(to + cc * 32, o);
                 tmem_wait_ld();
+                if (persist) {
+                    // The next item's Q and K/V are landing in shared memory: rows go
+                    // straight from registers (direct mode).
+                    if (!valid) continue;
+                    if (p.out_bf16) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            static_cast<__nv_bfloat16 *>(p.out) + row * D + cc * 32);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_uint4(pack_bf16(__uint_as_float(o[8 * k + 0]) * inv,
+                                                          __uint_as_float(o[8 * k + 1]) * inv),
+                                                pack_bf16(__uint_as_float(o[8 * k + 2]) * inv,
+                                                          __uint_as_float(o[8 * k + 3]) * inv),
+                                                pack_bf16(__uint_as_float(o[8 * k + 4]) * inv,
+                                                          __uint_as_float(o[8 * k + 5]) * inv),
+                                                pack_bf16(__uint_as_float(o[8 * k + 6]) * inv,
+                                                          __uint_as_float(o[8 * k + 7]) * inv));
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
+                                                                 row * D + cc * 32);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv,
+                                                 __uint_as_float(o[4 * k + 1]) * inv,
+                                                 __uint_as_float(o[4 * k + 2]) * inv,
+                                                 __uint_as_float(o[4 * k + 3]) * inv);
+                    }
+                    continue;
+                }
                 if (wide) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
@@ -787,6 +975,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                                                __uint_as_float(o[8 * k + 7]) * inv));
                 }
             }
+            // O is read out: the next item's first PV may overwrite it.
+            if (persist) mbar_arrive(BAR(C::B_OFREE + x));
             __syncwarp();
             // Byte offset of this thread's row in its destination, -1 for a row that
             // is not written.
@@ -797,7 +987,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             const int rpi = 32 / cpr;      // rows per store instruction
             const int ch = lane % cpr;     // this lane's chunk of its row
 #pragma unroll 1
-            for (int r0 = 0; r0 < 32; r0 += rpi) {
+            for (int r0 = 0; r0 < 32 && !persist; r0 += rpi) {
                 const int r = r0 + lane / cpr;
                 const int64_t off = __shfl_sync(0xffffffffu, my_off, r);
                 const uint4 v = ld_shared_v4(stage + (uint32_t)(r * rb + ((ch ^ (r & 7)) * 16)));
@@ -817,6 +1007,21 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 p.ws_ml[slot * 2] = p.ws_ml[slot * 2 + 1] = __int_as_float(0x7fc00000);
             } else {
                 nan_row<D>(p, b, hkv, f);
+            }
+        }
+        g += nb;
+        }
+        // After an abort, the items this warpgroup did not reach: their rows NaN.
+        for (; it < n_items; ++it) {
+            if ((skip >> it) & 1) continue;
+            const TcWork &w = PERSIST ? items[it] : w0;
+            const int f = (w.t0 + x * w.tstep) * BM + r;
+            if (f >= w.rows_unit || f % p.q_len >= w.qn) continue;
+            if (p.split) {
+                float *ml = p.ws_ml + (tile_row(p, w.b, w.hkv, f) * p.n_chunks + w.c) * 2;
+                ml[0] = ml[1] = __int_as_float(0x7fc00000);
+            } else {
+                nan_row<D>(p, w.b, w.hkv, f);
             }
         }
     }
@@ -840,14 +1045,38 @@ cudaError_t launch_instance(const TcParams &p, const CUtensorMap &tmQ, const CUt
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 64 && !configured[dev]) {
-        err = cudaFuncSetAttribute(fmha_tc_kernel<NT, D>,
+        err = cudaFuncSetAttribute(fmha_tc_kernel<NT, D, false>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if constexpr (NT == 2) {
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(fmha_tc_kernel<NT, D, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        }
         if (err != cudaSuccess) return err;
         configured[dev] = 1;
     }
     const int tiles = p.B * p.Hkv * p.tiles_per_unit;
     dim3 grid = p.split ? dim3(p.n_chunks, tiles, 1) : dim3(tiles / NT, 1, 1);
-    fmha_tc_kernel<NT, D><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, p);
+    TcParams q = p;
+    q.persistent = 0;
+    // Direct prefill with more tile pairs than SMs: one CTA per SM walks several
+    // (at most kMaxItems), so that CTA start-up, the first loads and the epilogue
+    // overlap the neighbouring items' work.
+    if (NT == 2 && !p.split && p.tiles_per_head > 0 && !p.q_lens) {
+        const int items = tiles / NT;
+        const int ctas = max(max(p.sms, 1), (items + kMaxItems - 1) / kMaxItems);
+        if (ctas < items) {
+            q.persistent = 1;
+            grid = dim3(ctas, 1, 1);
+        }
+    }
+    if constexpr (NT == 2) {
+        if (q.persistent) {
+            fmha_tc_kernel<NT, D, true><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, q);
+            return cudaGetLastError();
+        }
+    }
+    fmha_tc_kernel<NT, D, false><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, q);
     return cudaGetLastError();
 }
 

@@ -115,6 +115,8 @@ struct TcParams {
     float *lse;
     float *ws_acc, *ws_ml;
     uint32_t *status;
+    int32_t sms;         // SM count (sizes the persistent grid)
+    int32_t persistent;  // set by the launcher: CTAs walk several direct-mode items
 };
 
 // Paged KV append (kv_append.cu).
