@@ -91,3 +91,30 @@ def test_persistent_prefill_bad_page_and_seq_len():
     assert torch.isnan(out[0, :, 256:]).all() and torch.isnan(out[2]).all()
     assert torch.equal(out[0, :, :256], clean[0, :, :256])
     assert torch.equal(out[1], clean[1])
+
+
+def draw(i):
+    import random
+    r = random.Random(7000 + i)
+    Hkv = r.choice([1, 2, 4])
+    G = r.choice([2, 4, 6, 8])
+    return dict(B=r.randint(1, 3), Hq=G * Hkv, Hkv=Hkv, D=r.choice([64, 128]),
+                P=r.choice([8, 16, 32, 64, 128]), S=128 * r.randint(1, 6),
+                sms=r.randint(1, 6), seed=8000 + i,
+                var=r.choice([{}, {}, {"window": r.randint(1, 500)}, {"softcap": 20.0}]))
+
+
+RANDOM = [draw(i) for i in range(16)]
+
+
+@pytest.mark.parametrize("c", RANDOM, ids=[label(c) for c in RANDOM])
+def test_persistent_prefill_random_shapes(c):
+    prob = inputs.make("prefill", c["B"], c["Hq"], c["Hkv"], c["D"], c["P"], [c["S"]] * c["B"],
+                       seed=c["seed"])
+    dev = prob.to(DEV)
+    grid = run_gpu(dev, out_dtype=torch.float32, debug_flags=DIRECT, **c["var"])
+    pers = run_gpu(dev, out_dtype=torch.float32, debug_flags=DIRECT, sm_count=c["sms"],
+                   **c["var"])
+    torch.cuda.synchronize()
+    assert torch.equal(grid, pers)
+    assert_parity(prob, pers, oracle_rows(prob, **c["var"]), label(c))
