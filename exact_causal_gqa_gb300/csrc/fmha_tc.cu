@@ -638,6 +638,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         const int q4 = warp % 4;                      // TMEM lane quadrant
         const int r = q4 * 32 + lane;
         const bool capped = p.softcap_log2 > 0.f;
+        const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;  // 32-byte stores
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
         const uint32_t to = tl + C::o_col(x);
         bool ok = true;
@@ -926,30 +927,48 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 tmem_wait_ld();
                 if (persist) {
                     // The next item's Q and K/V are landing in shared memory: rows go
-                    // straight from registers (direct mode).
+                    // straight from registers (direct mode), in 32-byte stores when the
+                    // output allows (each fills a whole sector of its row).
                     if (!valid) continue;
+                    uint8_t *dst = static_cast<uint8_t *>(p.out) +
+                                   (row * D + cc * 32) * (p.out_bf16 ? 2 : 4);
+                    auto f = [&](int e) { return __uint_as_float(o[e]) * inv; };
                     if (p.out_bf16) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            static_cast<__nv_bfloat16 *>(p.out) + row * D + cc * 32);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            dst[k] = make_uint4(pack_bf16(__uint_as_float(o[8 * k + 0]) * inv,
-                                                          __uint_as_float(o[8 * k + 1]) * inv),
-                                                pack_bf16(__uint_as_float(o[8 * k + 2]) * inv,
-                                                          __uint_as_float(o[8 * k + 3]) * inv),
-                                                pack_bf16(__uint_as_float(o[8 * k + 4]) * inv,
-                                                          __uint_as_float(o[8 * k + 5]) * inv),
-                                                pack_bf16(__uint_as_float(o[8 * k + 6]) * inv,
-                                                          __uint_as_float(o[8 * k + 7]) * inv));
+                        for (int k = 0; k < 2; ++k) {  // 16 columns = 32 bytes each
+                            const uint4 a = make_uint4(
+                                pack_bf16(f(16 * k + 0), f(16 * k + 1)),
+                                pack_bf16(f(16 * k + 2), f(16 * k + 3)),
+                                pack_bf16(f(16 * k + 4), f(16 * k + 5)),
+                                pack_bf16(f(16 * k + 6), f(16 * k + 7)));
+                            const uint4 b = make_uint4(
+                                pack_bf16(f(16 * k + 8), f(16 * k + 9)),
+                                pack_bf16(f(16 * k + 10), f(16 * k + 11)),
+                                pack_bf16(f(16 * k + 12), f(16 * k + 13)),
+                                pack_bf16(f(16 * k + 14), f(16 * k + 15)));
+                            if (out32) {
+                                st_global_v8(dst + 32 * k, a, b);
+                            } else {
+                                reinterpret_cast<uint4 *>(dst + 32 * k)[0] = a;
+                                reinterpret_cast<uint4 *>(dst + 32 * k)[1] = b;
+                            }
+                        }
                     } else {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
-                                                                 row * D + cc * 32);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv,
-                                                 __uint_as_float(o[4 * k + 1]) * inv,
-                                                 __uint_as_float(o[4 * k + 2]) * inv,
-                                                 __uint_as_float(o[4 * k + 3]) * inv);
+                        for (int k = 0; k < 4; ++k) {  // 8 columns = 32 bytes each
+                            const uint4 a = make_uint4(
+                                __float_as_uint(f(8 * k + 0)), __float_as_uint(f(8 * k + 1)),
+                                __float_as_uint(f(8 * k + 2)), __float_as_uint(f(8 * k + 3)));
+                            const uint4 b = make_uint4(
+                                __float_as_uint(f(8 * k + 4)), __float_as_uint(f(8 * k + 5)),
+                                __float_as_uint(f(8 * k + 6)), __float_as_uint(f(8 * k + 7)));
+                            if (out32) {
+                                st_global_v8(dst + 32 * k, a, b);
+                            } else {
+                                reinterpret_cast<uint4 *>(dst + 32 * k)[0] = a;
+                                reinterpret_cast<uint4 *>(dst + 32 * k)[1] = b;
+                            }
+                        }
                     }
                     continue;
                 }

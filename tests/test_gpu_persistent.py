@@ -118,3 +118,20 @@ def test_persistent_prefill_random_shapes(c):
     torch.cuda.synchronize()
     assert torch.equal(grid, pers)
     assert_parity(prob, pers, oracle_rows(prob, **c["var"]), label(c))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_persistent_prefill_output_only_16_byte_aligned(dtype):
+    # the epilogue writes 32-byte pieces when the output allows; an output that is
+    # only 16-byte aligned takes 16-byte stores with the same values
+    prob = inputs.make("prefill", 2, 8, 2, 128, 64, [384, 384], seed=54)
+    dev = prob.to(DEV)
+    n = prob.q.numel()
+    shift = 16 // torch.tensor([], dtype=dtype).element_size()
+    buf = torch.empty(n + shift, dtype=dtype, device=DEV)
+    out = buf[shift:].view(prob.q.shape)
+    assert out.data_ptr() % 32 == 16
+    aligned = run_gpu(dev, out_dtype=dtype, debug_flags=DIRECT, sm_count=3)
+    run_gpu(dev, out_dtype=dtype, debug_flags=DIRECT, sm_count=3, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(aligned, out)
