@@ -12,6 +12,9 @@
 // block skipping, CPUAttn README: the fused QK -> RowNorm -> PV tile pipeline
 // stops at the last reachable K block) -- and folds each block into per-row
 // online-softmax state (the page fold of the CFR-Atlas README, "Core contract").
+// A direct prefill with more tile pairs than SMs runs persistent CTAs instead (the
+// PERSIST instance): one per SM, each walking its share of the tile pairs with every
+// role's barrier phases running on from one item to the next.
 //
 // Warp roles (128 + NT*128 threads, one CTA per SM):
 //   warp 0    TMA producer: the Q tiles once, then K blocks gathered page by page
@@ -30,8 +33,10 @@
 //             when the row max grew by more than 2^8 (exact: acc and l always
 //             share the reference max); write P as bf16 over its own S columns
 //             (plus the bf16 remainder P - bf16(P) for tiles whose rows see few
-//             keys, so that PV keeps ~16 bits of P there).  Epilogue: O / l,
-//             written row by row through shared memory.
+//             keys, so that PV keeps ~16 bits of P there); the row max comes from
+//             the TMEM loads themselves (tcgen05.ld.red).  Epilogue: O / l, written
+//             row by row through shared memory (persistent CTAs: straight from
+//             registers, the next item's Q being on its way into that memory).
 // Every mbarrier wait is bounded; a CTA that gives up records ATLAS_DEV_TIMEOUT,
 // lets its copies and MMAs finish, frees TMEM and writes NaN.
 #include "internal.h"
