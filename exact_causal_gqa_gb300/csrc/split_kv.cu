@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
         const uint64_t policy = policy_evict_first();
         const int BR = p.P < BT ? p.P : BT;  // rows per box
         const int subs = BT / BR;           // boxes per block (<= 8)
-        PageIdCache pages{p.page_table + (int64_t)b * p.max_pages, (kv_end - 1) / p.P};
+        const int lp = 31 - __clz(p.P);     // log2(P)
+        PageIdCache pages{p.page_table + (int64_t)b * p.max_pages, (kv_end - 1) >> lp};
         int issued = 0;
         for (int j = 0; j < nblocks; ++j) {
             const int s = j % STAGES;
@@ -333,14 +334,15 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
                 failed = true;
                 break;
             }
+            // A block starts on a multiple of 64 keys: with P <= 64 box sb is page
+            // t0 / P + sb from its first row, else the block lies inside one page.
+            // The block's pages share one 32-page line of the cache, so lane sb
+            // finds its page with one shuffle.
             const int t0 = kv_begin + j * BT;
             const int nsub = min(subs, (kv_end - t0 + BR - 1) / BR);
-            int my_y = 0;
-            for (int sb = 0; sb < nsub; ++sb) {
-                const int t = t0 + sb * BR;
-                const int y = (pages.get(t / p.P) * p.Hkv + hkv) * p.P + (t % p.P);
-                if (lane == sb) my_y = y;
-            }
+            const int my_y =
+                (pages.get_line(t0 >> lp, lane < nsub ? lane : 0) * p.Hkv + hkv) * p.P +
+                ((t0 + (lane < nsub ? lane : 0) * BR) & (p.P - 1));
             if ((p.debug_flags & ATLAS_DEBUG_WITHHOLD_STAGE) && j == 0) continue;
             if (lane < nsub) {
                 if (lane == 0)
