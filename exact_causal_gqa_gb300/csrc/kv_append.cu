@@ -21,7 +21,9 @@ constexpr int kUnroll = 4;
 
 template <typename I>
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
-    const I vec = (I)(p.row_bytes / 16);  // 16-byte pieces per row
+    const I vec = (I)(p.row_bytes / 16);  // 16-byte pieces per row: 8, 16 or 32
+    const int lvec = 31 - __clz((int)vec);
+    const int lp = 31 - __clz(p.P);       // page_tokens is a power of two
     const I total = (I)p.B * (I)p.Hkv * (I)p.max_new * vec;
     const I stride = (I)gridDim.x * (I)blockDim.x;
     const char *kn = static_cast<const char *>(p.k_new);
@@ -37,8 +39,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
             dst[u] = -1;
             const I idx = base + (I)u * stride;
             if (idx >= total) continue;
-            const int piece = (int)(idx % vec);
-            const I row = idx / vec;  // (b, g, j)
+            const int piece = (int)(idx & (vec - 1));
+            const I row = idx >> lvec;  // (b, g, j)
             const int j = (int)(row % (I)p.max_new);
             const I bg = row / (I)p.max_new;
             const int g = (int)(bg % (I)p.Hkv);
@@ -55,13 +57,14 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
                 if (p.status && piece == 0) atomicOr(p.status, ATLAS_DEV_BAD_SEQLEN);
                 continue;
             }
-            const int page = p.page_table[(int64_t)b * p.max_pages + t / p.P];
+            const int page = p.page_table[(int64_t)b * p.max_pages + (t >> lp)];
             if (page < 0 || page >= p.num_pages) {
                 if (p.status && piece == 0) atomicOr(p.status, ATLAS_DEV_BAD_PAGE);
                 continue;
             }
             const int64_t src = (int64_t)row * p.row_bytes + piece * 16;
-            dst[u] = (((int64_t)page * p.Hkv + g) * p.P + t % p.P) * p.row_bytes + piece * 16;
+            dst[u] = (((int64_t)page * p.Hkv + g) * p.P + (t & (p.P - 1))) * p.row_bytes +
+                     piece * 16;
             kd[u] = *reinterpret_cast<const uint4 *>(kn + src);
             vd[u] = *reinterpret_cast<const uint4 *>(vn + src);
         }

@@ -770,6 +770,7 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
     float *wK = sW + warp * Lay::kWarp;
     float *wV = wK + 2 * Lay::kBuf;
     float *wP = wK + 4 * Lay::kBuf;
+    const int lp = 31 - __clz(p.P);  // log2(P): P is a power of two
     auto load = [&](int kb, int buf) {
         const uint32_t kd = smem_u32(wK + buf * Lay::kBuf), vd = smem_u32(wV + buf * Lay::kBuf);
         for (int idx = lane; idx < BK * DV4; idx += 32) {
@@ -777,7 +778,8 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
             const int t = kb + kr;
             const bool in = t < kv_end;
             const int tt = in ? t : kv_begin;
-            const int64_t row = ((int64_t)ptab[tt / p.P] * p.Hkv + hkv) * p.P + tt % p.P;
+            const int64_t row =
+                ((int64_t)ptab[tt >> lp] * p.Hkv + hkv) * p.P + (tt & (p.P - 1));
             const uint32_t off = (uint32_t)(kr * Lay::KS + 4 * d4) * 4u;
             cp_async16(kd + off, kp + row * D + 4 * d4, in ? 16u : 0u);
             cp_async16(vd + off, vp + row * D + 4 * d4, in ? 16u : 0u);
