@@ -42,9 +42,8 @@ __device__ __forceinline__ bool seq_len_bad(const SplitParams &p, int L, int qn)
 
 // Flat output row of column n of (b, hkv).
 __device__ __forceinline__ int64_t column_row(const SplitParams &p, int b, int hkv, int n) {
-    const int h = hkv * p.G + n / p.q_len;
-    const int i = n % p.q_len;
-    return ((int64_t)b * p.Hq + h) * p.q_len + i;
+    // q head hkv * G + n / q_len, row n % q_len: together (hkv * G) * q_len + n
+    return ((int64_t)b * p.Hq + (int64_t)hkv * p.G) * p.q_len + n;
 }
 
 // Keys visible to column n (absolute count), as defined by the suffix rule.  L
