@@ -1000,7 +1000,10 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 }
             }
             // O is read out: the next item's first PV may overwrite it.
-            if (persist) mbar_arrive(BAR(C::B_OFREE + x));
+            if (persist) {
+                tc_fence_before();  // the O loads are ordered before the arrival
+                mbar_arrive(BAR(C::B_OFREE + x));
+            }
             __syncwarp();
             // Byte offset of this thread's row in its destination, -1 for a row that
             // is not written.
