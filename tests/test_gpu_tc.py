@@ -235,3 +235,25 @@ def test_suffix_batch_past_the_longest_first_order(dtype):
     assert_parity(prob, out, ref, f"B{B} {dtype}")
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.reshape(-1), rtol=0,
                                atol=2e-4 if dtype == "bf16" else 2e-5)
+
+
+@pytest.mark.parametrize("kind,lens,q_len,outlier,scale", [
+    ("prefill", [2048], 2048, (0.02, 3.0), None),
+    ("prefill", [2048], 2048, (0.002, 4.0), None),
+    ("prefill", [2048], 2048, (0.0, 1.0), 1.15),
+    ("prefill", [2048], 2048, (0.0, 1.0), 1.24),
+    ("suffix", [3000, 5000], 64, (0.002, 4.0), None),
+    ("suffix", [3000, 5000], 64, (0.02, 3.0), None),
+])
+def test_hilo_threshold_margin(kind, lens, q_len, outlier, scale):
+    # The inputs that came closest to the bound when the per-block hi + lo threshold was
+    # chosen (outlier K rows, scores as sharp as the limit above which every block takes
+    # hi + lo): the largest error must keep a margin of 2 to 2e-3.
+    prob = inputs.make(kind, len(lens), 8, 2, 128, 64, lens, q_len=q_len, seed=102,
+                       k_outlier_prob=outlier[0], k_outlier_scale=outlier[1],
+                       scale=None if scale is None else scale / np.sqrt(128))
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32,
+                  debug_flags=atlas.DEBUG_TC_DIRECT if kind == "prefill" else 0)
+    torch.cuda.synchronize()
+    err = assert_parity(prob, out, oracle_rows(prob), kind)
+    assert err <= 1e-3, f"{kind}: max err {err:.3e} leaves less than a 2x margin"
