@@ -267,7 +267,6 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     // every role walks them, and the barrier phases run on across items (counted in
     // blocks and items), so the next item's Q, K/V and first S products overlap the
     // current item's last blocks and epilogue.
-    constexpr bool persist = PERSIST;
     int n_items = 1;
     TcWork w0{};
     if (PERSIST) {
@@ -932,7 +931,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 uint32_t o[32];
                 tmem_ld32(to + cc * 32, o);
                 tmem_wait_ld();
-                if (persist) {
+                if (PERSIST) {
                     // The next item's Q and K/V are landing in shared memory: rows go
                     // straight from registers (direct mode), in 32-byte stores when the
                     // output allows (each fills a whole sector of its row).
@@ -1002,7 +1001,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                 }
             }
             // O is read out: the next item's first PV may overwrite it.
-            if (persist) {
+            if (PERSIST) {
                 tc_fence_before();  // the O loads are ordered before the arrival
                 mbar_arrive(BAR(C::B_OFREE + x));
             }
@@ -1016,7 +1015,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             const int rpi = 32 / cpr;      // rows per store instruction
             const int ch = lane % cpr;     // this lane's chunk of its row
 #pragma unroll 1
-            for (int r0 = 0; r0 < 32 && !persist; r0 += rpi) {
+            for (int r0 = 0; r0 < 32 && !PERSIST; r0 += rpi) {
                 const int r = r0 + lane / cpr;
                 const int64_t off = __shfl_sync(0xffffffffu, my_off, r);
                 const uint4 v = ld_shared_v4(stage + (uint32_t)(r * rb + ((ch ^ (r & 7)) * 16)));
@@ -1086,26 +1085,25 @@ cudaError_t launch_instance(const TcParams &p, const CUtensorMap &tmQ, const CUt
     }
     const int tiles = p.B * p.Hkv * p.tiles_per_unit;
     dim3 grid = p.split ? dim3(p.n_chunks, tiles, 1) : dim3(tiles / NT, 1, 1);
-    TcParams q = p;
-    q.persistent = 0;
     // Direct prefill with more tile pairs than SMs: one CTA per SM walks several
     // (at most kMaxItems), so that CTA start-up, the first loads and the epilogue
     // overlap the neighbouring items' work.
+    bool persistent = false;
     if (NT == 2 && !p.split && p.tiles_per_head > 0 && !p.q_lens) {
         const int items = tiles / NT;
         const int ctas = max(max(p.sms, 1), (items + kMaxItems - 1) / kMaxItems);
         if (ctas < items) {
-            q.persistent = 1;
+            persistent = true;
             grid = dim3(ctas, 1, 1);
         }
     }
     if constexpr (NT == 2) {
-        if (q.persistent) {
-            fmha_tc_kernel<NT, D, true><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, q);
+        if (persistent) {
+            fmha_tc_kernel<NT, D, true><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, p);
             return cudaGetLastError();
         }
     }
-    fmha_tc_kernel<NT, D, false><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, q);
+    fmha_tc_kernel<NT, D, false><<<grid, C::kThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 

@@ -115,8 +115,7 @@ struct TcParams {
     float *lse;
     float *ws_acc, *ws_ml;
     uint32_t *status;
-    int32_t sms;         // SM count (sizes the persistent grid)
-    int32_t persistent;  // set by the launcher: CTAs walk several direct-mode items
+    int32_t sms;         // SM count (sizes the persistent prefill grid)
 };
 
 // Paged KV append (kv_append.cu).
