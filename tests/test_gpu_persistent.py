@@ -135,3 +135,31 @@ def test_persistent_prefill_output_only_16_byte_aligned(dtype):
     run_gpu(dev, out_dtype=dtype, debug_flags=DIRECT, sm_count=3, out=out)
     torch.cuda.synchronize()
     assert torch.equal(aligned, out)
+
+
+@pytest.mark.parametrize("S", [4096, 4224])
+def test_persistent_prefill_full_item_lists(S):
+    # 128 tile pairs with one SM allowed: two CTAs of exactly 64 items each (the
+    # per-CTA limit, every bit of the item mask in use); 132 pairs: three CTAs
+    prob = inputs.make("prefill", 1, 8, 2, 128, 64, [S], seed=55)
+    dev = prob.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    grid = run_gpu(dev, out_dtype=torch.float32, debug_flags=DIRECT)
+    pers = run_gpu(dev, out_dtype=torch.float32, debug_flags=DIRECT, sm_count=1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(grid, pers)
+    assert_parity(prob, pers, oracle_rows(prob), f"S{S}")
+
+
+def test_persistent_prefill_every_item_skipped():
+    # a bad seq_len makes all 64 items of both CTAs skip: the rows are NaN, the
+    # status says why, and the CTAs leave before their setup
+    prob = inputs.make("prefill", 1, 8, 2, 128, 64, [4096], seed=56)
+    prob.seq_lens[0] = 4095
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(prob.to(DEV), out_dtype=torch.float32, debug_flags=DIRECT, sm_count=1,
+                  status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == atlas.DEV_BAD_SEQLEN
+    assert torch.isnan(out).all()
