@@ -574,17 +574,31 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 
 // ---------------------------------------------------------------- cluster merge
 // Cluster mode: the n_chunks splits of one (sequence, kv head, column tile) are the
-// CTAs of one thread-block cluster (rank = split index).  Each leaves its partial
-// state in its own shared memory; the CTAs then read them through distributed
-// shared memory and apply the structured merge (CPUAttn README, "Operator model")
-// to a share of the output elements each, with the merge kernel's arithmetic in
-// split order, so the bits equal split + merge.
-// No workspace, no second launch.  Every CTA reaches both cluster barriers on every
-// path (no early exit in this mode), and the loops before them are bounded.
+// CTAs of one thread-block cluster (rank = split index).  Each CTA keeps its partial
+// state in slot `rank` of a per-CTA array of kClusterSlots slots, and every CTA but
+// rank 0 copies it into the same slot of rank 0 through distributed shared memory.
+// After one cluster barrier, rank 0 alone applies the structured merge (CPUAttn
+// README, "Operator model") to every output element, reading the slots locally,
+// with the merge kernel's arithmetic in split order, so the bits equal split + merge;
+// the other CTAs leave at that barrier.  No workspace, no second launch.
+// Every CTA arrives on the cluster barrier at entry (nothing may write into a CTA
+// of the cluster before all of them have started) and reaches both barrier phases
+// on every path (no early exit in this mode); the loops before them are bounded.
+constexpr int kClusterSlots = 8;  // the portable cluster size
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
+}
+
+// The first phase of the cluster barrier, split: every thread arrives at entry and
+// waits just before its first write into another CTA.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_barrier() {
@@ -593,86 +607,87 @@ __device__ __forceinline__ void cluster_barrier() {
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 32-bit load from the shared memory of CTA `rank` of this cluster, at the offset
+// 16-byte store into the shared memory of CTA `rank` of this cluster, at the offset
 // that `local` (a shared-memory address of this CTA) has in its own.
-__device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
+__device__ __forceinline__ void st_cluster_v4(uint32_t local, uint32_t rank, float4 v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
 }
 
+// slots: this CTA's kClusterSlots x [NCOLS][D + 2] array; this CTA's state is in slot
+// `rank` (written before the call).
 template <int NCOLS, int D>
-__device__ void cluster_merge(const SplitParams &p, const float *part, int col0, int ncols,
-                              int qn, bool bad_len, int seq_len) {
-    constexpr int kMaxSplits = 8;  // the portable cluster size
-    __syncthreads();
-    cluster_barrier();  // every split's state is in its CTA's shared memory
-    {
-        // The output rows' elements are shared out over every CTA of the cluster;
-        // each element's loads from all splits are issued before any is used.
-        const int b = blockIdx.z;
-        const int hkv = blockIdx.y / p.col_tiles;
-        const int L = seq_len;  // seq_lens[b], read at the kernel's start
-        const uint32_t base = smem_u32(part);
-        const int rank = (int)cluster_ctarank();
-        for (int idx = rank * (int)blockDim.x + (int)threadIdx.x; idx < ncols * D;
-             idx += p.n_chunks * (int)blockDim.x) {
-            const int c = idx / D, d = idx % D;
-            const int i = (col0 + c) % p.q_len;
-            if (!bad_len && i >= qn) continue;  // padding row: not written
-            const int64_t row = column_row(p, b, hkv, col0 + c);
-            float o = __int_as_float(0x7fc00000), lse = o;
-            if (!bad_len) {
-                const int visible = L - qn + i + 1;
-                // splits holding this row's keys: [first, nsplit)
-                const int first = p.window > 0 ? max(0, visible - p.window) / p.chunk : 0;
-                const int nsplit = min((visible + p.chunk - 1) / p.chunk, p.n_chunks);
-                const uint32_t am = base + (uint32_t)(c * (D + 2) + D) * 4u;
-                const uint32_t aa = base + (uint32_t)(c * (D + 2) + d) * 4u;
-                float m[kMaxSplits], l[kMaxSplits], a[kMaxSplits];
+__device__ void cluster_merge(const SplitParams &p, float *slots, int col0, int ncols, int qn,
+                              bool bad_len, int seq_len) {
+    constexpr int kSlot = NCOLS * (D + 2);  // floats, a multiple of 4
+    static_assert(kSlot % 4 == 0, "16-byte slot copies");
+    const uint32_t rank = cluster_ctarank();
+    __syncthreads();  // this CTA's state is in its slot
+    cluster_wait();   // every CTA of the cluster has started
+    if (rank != 0) {
+        const float4 *mine = reinterpret_cast<const float4 *>(slots + rank * kSlot);
+        const uint32_t dst = smem_u32(slots + rank * kSlot);
+        for (int i = threadIdx.x; i < kSlot / 4; i += blockDim.x)
+            st_cluster_v4(dst + (uint32_t)i * 16u, 0u, mine[i]);
+    }
+    cluster_barrier();  // rank 0 sees every split's state
+    if (rank != 0) return;
+    const int b = blockIdx.z;
+    const int hkv = blockIdx.y / p.col_tiles;
+    const int L = seq_len;  // seq_lens[b], read at the kernel's start
+    for (int idx = threadIdx.x; idx < ncols * D; idx += blockDim.x) {
+        const int c = idx / D, d = idx % D;
+        const int i = (col0 + c) % p.q_len;
+        if (!bad_len && i >= qn) continue;  // padding row: not written
+        const int64_t row = column_row(p, b, hkv, col0 + c);
+        float o = __int_as_float(0x7fc00000), lse = o;
+        if (!bad_len) {
+            const int visible = L - qn + i + 1;
+            // splits holding this row's keys: [first, nsplit)
+            const int first = p.window > 0 ? max(0, visible - p.window) / p.chunk : 0;
+            const int nsplit = min((visible + p.chunk - 1) / p.chunk, p.n_chunks);
+            float m[kClusterSlots], l[kClusterSlots], a[kClusterSlots];
 #pragma unroll
-                for (int u = 0; u < kMaxSplits; ++u) {
-                    m[u] = l[u] = a[u] = 0.f;
-                    if (first + u < nsplit) {
-                        m[u] = ld_cluster_f32(am, first + u);
-                        l[u] = ld_cluster_f32(am + 4, first + u);
-                        a[u] = ld_cluster_f32(aa, first + u);
-                    }
-                }
-                const float sink2 =
-                    p.sinks ? p.sinks[(row / p.q_len) % p.Hq] * kLog2e : -INFINITY;
-                float M = sink2;
-                bool has_nan = isnan(sink2);
-#pragma unroll
-                for (int u = 0; u < kMaxSplits; ++u) {
-                    if (first + u >= nsplit) break;
-                    if (isnan(l[u]) || isnan(m[u])) has_nan = true;
-                    else if (l[u] > 0.f) M = fmaxf(M, m[u]);
-                }
-                if (!has_nan && M != -INFINITY) {
-                    float lsum = p.sinks ? ex2(sink2 - M) : 0.f, acc = 0.f;
-#pragma unroll
-                    for (int u = 0; u < kMaxSplits; ++u) {
-                        if (first + u >= nsplit) break;
-                        const float w = l[u] > 0.f ? ex2(m[u] - M) : 0.f;
-                        lsum = fmaf(w, l[u], lsum);
-                        acc = fmaf(w, a[u], acc);
-                    }
-                    o = acc / lsum;
-                    lse = kLn2 * (M + log2f(lsum));
+            for (int u = 0; u < kClusterSlots; ++u) {
+                m[u] = l[u] = a[u] = 0.f;
+                if (first + u < nsplit) {
+                    const float *st = slots + (first + u) * kSlot + c * (D + 2);
+                    m[u] = st[D];
+                    l[u] = st[D + 1];
+                    a[u] = st[d];
                 }
             }
-            if (p.out_bf16)
-                static_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(o);
-            else
-                static_cast<float *>(p.out)[row * D + d] = o;
-            if (d == 0 && p.lse) p.lse[row] = lse;
+            const float sink2 = p.sinks ? p.sinks[(row / p.q_len) % p.Hq] * kLog2e : -INFINITY;
+            float M = sink2;
+            bool has_nan = isnan(sink2);
+#pragma unroll
+            for (int u = 0; u < kClusterSlots; ++u) {
+                if (first + u >= nsplit) break;
+                if (isnan(l[u]) || isnan(m[u])) has_nan = true;
+                else if (l[u] > 0.f) M = fmaxf(M, m[u]);
+            }
+            if (!has_nan && M != -INFINITY) {
+                float lsum = p.sinks ? ex2(sink2 - M) : 0.f, acc = 0.f;
+#pragma unroll
+                for (int u = 0; u < kClusterSlots; ++u) {
+                    if (first + u >= nsplit) break;
+                    const float w = l[u] > 0.f ? ex2(m[u] - M) : 0.f;
+                    lsum = fmaf(w, l[u], lsum);
+                    acc = fmaf(w, a[u], acc);
+                }
+                o = acc / lsum;
+                lse = kLn2 * (M + log2f(lsum));
+            }
         }
+        if (p.out_bf16)
+            static_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(o);
+        else
+            static_cast<float *>(p.out)[row * D + d] = o;
+        if (d == 0 && p.lse) p.lse[row] = lse;
     }
-    __syncthreads();
-    cluster_barrier();  // every CTA has read the states it needs before any exits
 }
 
 // ---------------------------------------------------------------- f32 path
@@ -700,8 +715,10 @@ struct F32Layout {
     static constexpr int kWarp = 4 * kBuf + kF32Keys * NC;  // K[2], V[2], P[key][col]
     static constexpr int kQ = NC * KS;
     static constexpr int kBytes = (kQ + W * kWarp) * 4;
-    // cluster mode only: this split's state per column, [NC][D + 2], after the rings
-    static constexpr int kPartBytes = NC * (D + 2) * 4;
+    // cluster mode only, after the rings: kClusterSlots splits' states, each
+    // [NC][D + 2] (rank 0 merges them; every other CTA uses its own slot only)
+    static constexpr int kPartBytes = kClusterSlots * NC * (D + 2) * 4;
+    static_assert(kBytes + kPartBytes <= 232448, "shared memory budget (cluster mode)");
     static_assert(2 * W * NC + W * NC * D <= W * kWarp, "combine scratch fits the rings");
 };
 
@@ -714,7 +731,9 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
     extern __shared__ __align__(16) float f32d_smem[];
     float *sQ = f32d_smem;
     float *sW = sQ + Lay::kQ;
-    float *part = sW + W * Lay::kWarp;  // cluster mode only
+    float *slots = sW + W * Lay::kWarp;  // cluster mode only
+    if (p.cluster) cluster_arrive_relaxed();  // first phase, waited on before any remote write
+    float *part = p.cluster ? slots + cluster_ctarank() * (NC * (D + 2)) : nullptr;
 
     const int b = blockIdx.z;
     const int hkv = blockIdx.y / p.col_tiles;
@@ -750,7 +769,7 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
         const float nan = __int_as_float(0x7fc00000);
         for (int idx = threadIdx.x; idx < NC * (D + 2); idx += W * 32)
             part[idx] = why == kBadPage ? nan : (idx % (D + 2) == D ? -INFINITY : 0.f);
-        cluster_merge<NC, D>(p, part, col0, ncols, qn, why == kBadLen, seq_len_b);
+        cluster_merge<NC, D>(p, slots, col0, ncols, qn, why == kBadLen, seq_len_b);
         return;
     }
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -933,7 +952,7 @@ __global__ void __launch_bounds__(F32Layout<D, NC>::W * 32, F32Layout<D, NC>::kM
     __syncthreads();
     if (p.cluster) {
         write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, qn, false, part);
-        cluster_merge<NC, D>(p, part, col0, ncols, qn, false, seq_len_b);
+        cluster_merge<NC, D>(p, slots, col0, ncols, qn, false, seq_len_b);
         return;
     }
     write_partials<W, NC, D>(p, cm, cl, cacc, col0, ncols, qn, false);
